@@ -1,0 +1,356 @@
+"""Seeded synthetic workloads for paged decode attention.
+
+This module only draws inputs: random K/V/Q values, context lengths, block
+tables (a random permutation of the pool), slot mappings and copy pairs.  It
+computes no attention and imports neither the oracle nor the CUDA library, so
+the tests can feed the same tensors to both.
+
+Workloads (sizes follow the paged-attention pages' setting: block pool
+``[num_blocks, block_size, heads, head_dim]``, one decode query per request):
+
+* ``c1``  fp32, 8 heads, head_dim 32, block_size 4, a pool of 16 blocks, one
+  request of 10 tokens over 3 blocks taken from a seeded permutation: the
+  worked example of "19.2 KV Cache 系统化管理" §19.2.3 with fixed seeds.
+* ``c2``  bf16 MHA 32 heads, D 128, bs 16, batch 64, lengths U[128, 2048],
+  plus the append of each request's newest token.
+* ``c3``  bf16 MHA 40 heads, D 128, bs 16, batch 128, lengths log-normal with
+  median 512 and sigma 1 (natural log), rounded, clipped to [1, 4096].
+* ``c4``  bf16 GQA 32/8 heads, D 128, bs 16 (``c4b32``: bs 32), batch 256,
+  lengths U[1024, 32768], split-K partitions of 512 tokens.
+* ``c5``  64 prompts x 8 samples sharing 1024-token prompts (64 full blocks,
+  reference count 8) with private tails U[0, 256]; GQA 32/8, D 128, bs 16.
+  Its copy-on-write case uses prompts of 1024 - r tokens (r ~ U[1, 15]) so
+  block 63 is a shared partial block that 7 of 8 samples copy; its prefill
+  case is a 512-query causal tile at positions 512..1023 of each prompt.
+
+Values are N(0, 1) drawn in fp32 by a seeded ``torch.Generator`` (on the
+device the case is built on) and rounded to the pool dtype.  Slots a sequence
+does not hold and unmapped blocks are filled with NaN when ``nan_fill`` is
+set, so any read of them shows up in the output.  Unused block-table entries
+hold ``num_blocks`` (out of range).
+"""
+
+from dataclasses import dataclass, field
+import math
+
+import numpy as np
+import torch
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@dataclass
+class Spec:
+    name: str
+    dtype: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    lens: tuple
+    partition: int = 512
+    spare: float = 1.25
+    pool: int = 0            # fixed pool size (0: derived from the lengths)
+    seed: int = 0
+
+
+SPECS = {
+    "c1": Spec("c1", "f32", 1, 8, 8, 32, 4, ("fixed", 10), partition=0, pool=16, seed=1),
+    "c2": Spec("c2", "bf16", 64, 32, 32, 128, 16, ("uniform", 128, 2048), seed=2),
+    "c3": Spec("c3", "bf16", 128, 40, 40, 128, 16, ("lognormal", 512, 1.0, 4096), seed=3),
+    "c4": Spec("c4", "bf16", 256, 32, 8, 128, 16, ("uniform", 1024, 32768), seed=4),
+    "c4b32": Spec("c4b32", "bf16", 256, 32, 8, 128, 32, ("uniform", 1024, 32768), seed=4),
+    "c5": Spec("c5", "bf16", 512, 32, 8, 128, 16, ("shared", 64, 8, 1024, 256), seed=5),
+}
+
+# Batch sizes small enough for the float64 oracle to finish in seconds while
+# still spanning several 512-token partitions and a ragged last block.
+SMALL_B = {"c1": 1, "c2": 6, "c3": 10, "c4": 3, "c4b32": 3, "c5": 16}
+
+
+@dataclass
+class DecodeCase:
+    spec: Spec
+    scale: float
+    q: torch.Tensor             # [B, Hq, D]
+    k_cache: torch.Tensor       # [NB, bs, Hkv, D]
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor  # [B, max_blocks] int32
+    context_lens: torch.Tensor  # [B] int32
+    key: torch.Tensor           # [T, Hkv, D] newest token per request
+    value: torch.Tensor
+    slot_mapping: torch.Tensor  # [T] int64
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def num_blocks(self):
+        return self.k_cache.shape[0]
+
+    @property
+    def max_blocks(self):
+        return self.block_tables.shape[1]
+
+
+def scale_for(D):
+    """1/sqrt(head_dim), rounded to fp32: the value handed to both sides."""
+    return float(np.float32(1.0 / math.sqrt(D)))
+
+
+def _lengths(spec, B, rng):
+    kind = spec.lens[0]
+    if kind == "fixed":
+        return np.full(B, spec.lens[1], dtype=np.int64)
+    if kind == "uniform":
+        return rng.integers(spec.lens[1], spec.lens[2], size=B, endpoint=True)
+    if kind == "lognormal":
+        med, sigma, cap = spec.lens[1:]
+        x = np.exp(rng.normal(math.log(med), sigma, size=B))
+        return np.clip(np.rint(x), 1, cap).astype(np.int64)
+    raise ValueError(kind)
+
+
+def _randn(shape, dtype, gen, device, chunk_rows=1 << 14):
+    """N(0,1) in fp32, rounded to ``dtype``; drawn in row chunks so full-size
+    pools never hold an fp32 copy of themselves."""
+    out = torch.empty(shape, dtype=dtype, device=device)
+    rows = shape[0]
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1] = torch.randn((r1 - r0,) + tuple(shape[1:]), generator=gen,
+                                 device=device, dtype=torch.float32).to(dtype)
+    return out
+
+
+def _generator(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _nan_unused(k, v, tables, lens, bs, nan_fill):
+    """NaN every slot no sequence holds: unmapped blocks and the tail slots of
+    each sequence's last block."""
+    if not nan_fill or not k.dtype.is_floating_point:
+        return
+    NB = k.shape[0]
+    used = torch.zeros(NB, dtype=torch.bool, device=k.device)
+    tails = []
+    for b in range(len(lens)):
+        n = -(-int(lens[b]) // bs)
+        used[tables[b, :n].long().to(k.device)] = True
+        valid = int(lens[b]) - (n - 1) * bs if n else 0
+        if n and valid < bs:
+            tails.append((int(tables[b, n - 1]), valid))
+    k[~used] = float("nan")
+    v[~used] = float("nan")
+    for blk, valid in tails:
+        k[blk, valid:] = float("nan")
+        v[blk, valid:] = float("nan")
+
+
+def _tables(lens, bs, NB_min, spare, rng, fixed_pool=0):
+    nblk = [-(-int(L) // bs) for L in lens]
+    total = sum(nblk)
+    NB = fixed_pool or max(NB_min, int(math.ceil(total * spare)) + len(lens))
+    perm = rng.permutation(NB)
+    maxb = max(1, max(nblk))
+    tables = np.full((len(lens), maxb), NB, dtype=np.int32)
+    off = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = perm[off:off + n]
+        off += n
+    return tables, NB, perm[off:]
+
+
+def decode_case(name, small=False, device="cpu", nan_fill=True, seed=None, B=None):
+    """Build one decode workload.  The pool holds every token of every context
+    except each sequence's newest one (position L-1), whose K/V arrive in
+    ``key``/``value`` with its slot in ``slot_mapping``: the caller appends,
+    then attends (context_lens count the newest token)."""
+    spec = SPECS[name]
+    seed = spec.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    if B is None:
+        B = SMALL_B[name] if small else spec.B
+    dt = DTYPES[spec.dtype]
+    gen = _generator(device, seed)
+    extra = {}
+
+    if spec.lens[0] == "shared":
+        return _shared_prefix_case(spec, B, rng, gen, device, nan_fill)
+
+    lens = _lengths(spec, B, rng)
+    max_len = spec.lens[1] if spec.lens[0] == "fixed" else spec.lens[-1]
+    tables, NB, _ = _tables(lens, spec.bs, 0, spec.spare, rng, spec.pool)
+    maxb = -(-int(max_len) // spec.bs)
+    if tables.shape[1] < maxb:
+        pad = np.full((B, maxb - tables.shape[1]), NB, dtype=np.int32)
+        tables = np.concatenate([tables, pad], axis=1)
+
+    k = _randn((NB, spec.bs, spec.Hkv, spec.D), dt, gen, device)
+    v = _randn((NB, spec.bs, spec.Hkv, spec.D), dt, gen, device)
+    q = _randn((B, spec.Hq, spec.D), dt, gen, device)
+    key = _randn((B, spec.Hkv, spec.D), dt, gen, device)
+    value = _randn((B, spec.Hkv, spec.D), dt, gen, device)
+    tables_t = torch.from_numpy(tables)
+    _nan_unused(k, v, tables_t, lens, spec.bs, nan_fill)
+    # The newest token's slot is not yet written: mark it like any free slot.
+    slots = np.array([int(tables[b, (L - 1) // spec.bs]) * spec.bs + (L - 1) % spec.bs
+                      for b, L in enumerate(lens)], dtype=np.int64)
+    if nan_fill and k.dtype.is_floating_point:
+        for s in slots:
+            k[s // spec.bs, s % spec.bs] = float("nan")
+            v[s // spec.bs, s % spec.bs] = float("nan")
+    return DecodeCase(spec, scale_for(spec.D), q, k, v,
+                      tables_t.to(device), torch.from_numpy(lens.astype(np.int32)).to(device),
+                      key, value, torch.from_numpy(slots).to(device), extra)
+
+
+def _shared_prefix_case(spec, n_seq, rng, gen, device, nan_fill):
+    """Parallel sampling over shared prompts (see the module docstring)."""
+    _, P_full, S, prefix, tail_max = spec.lens
+    S_eff = min(S, n_seq)
+    P = max(1, n_seq // S_eff)
+    B = P * S_eff
+    bs = spec.bs
+    tails = rng.integers(0, tail_max, size=B, endpoint=True)
+    lens = prefix + tails
+    pre_blocks = prefix // bs
+    n_tail_blocks = [-(-int(t) // bs) for t in tails]
+    total = P * pre_blocks + sum(n_tail_blocks)
+    # spare room for copy-on-write blocks (7 per prompt) and later appends
+    NB = int(math.ceil(total * spec.spare)) + P * S_eff + B
+    perm = rng.permutation(NB)
+    maxb = pre_blocks + -(-tail_max // bs)
+    tables = np.full((B, maxb), NB, dtype=np.int32)
+    off = 0
+    prompt_blocks = []
+    for p in range(P):
+        pb = perm[off:off + pre_blocks]
+        off += pre_blocks
+        prompt_blocks.append(pb)
+        for s in range(S_eff):
+            b = p * S_eff + s
+            tables[b, :pre_blocks] = pb
+            n = n_tail_blocks[b]
+            tables[b, pre_blocks:pre_blocks + n] = perm[off:off + n]
+            off += n
+    free_blocks = perm[off:]
+    dt = DTYPES[spec.dtype]
+    k = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    v = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    q = _randn((B, spec.Hq, spec.D), dt, gen, device)
+    key = _randn((B, spec.Hkv, spec.D), dt, gen, device)
+    value = _randn((B, spec.Hkv, spec.D), dt, gen, device)
+    tables_t = torch.from_numpy(tables)
+    _nan_unused(k, v, tables_t, lens, bs, nan_fill)
+    slots = np.array([int(tables[b, (L - 1) // bs]) * bs + (L - 1) % bs
+                      for b, L in enumerate(lens)], dtype=np.int64)
+    # A sequence with no private tail would write into a shared prompt block;
+    # this case keeps appends private by not appending for those sequences.
+    slots[tails == 0] = -1
+    if nan_fill:
+        for s in slots[slots >= 0]:
+            k[s // bs, s % bs] = float("nan")
+            v[s // bs, s % bs] = float("nan")
+    extra = {"prompts": P, "samples": S_eff, "prefix": prefix, "tails": tails,
+             "prompt_blocks": np.stack(prompt_blocks), "free_blocks": free_blocks}
+    return DecodeCase(spec, scale_for(spec.D), q, k, v,
+                      tables_t.to(device), torch.from_numpy(lens.astype(np.int32)).to(device),
+                      key, value, torch.from_numpy(slots).to(device), extra)
+
+
+def cow_case(small=False, device="cpu", seed=None, prompts=None):
+    """Copy-on-write workload: prompts of 1024 - r tokens (r ~ U[1, 15]) whose
+    last prompt block is partial and shared by 8 samples.  Returns the pool,
+    the per-prompt shared block ids and the (src, dst) pairs that give 7 of
+    the 8 samples a private copy before their first append.  Pairs are drawn
+    from the free blocks in a seeded order."""
+    spec = SPECS["c5"]
+    seed = (spec.seed if seed is None else seed) + 100
+    rng = np.random.default_rng(seed)
+    P = prompts or (4 if small else 64)
+    S = spec.lens[2]
+    bs = spec.bs
+    r = rng.integers(1, 15, size=P, endpoint=True)
+    plen = spec.lens[3] - r
+    pre_blocks = -(-spec.lens[3] // bs)
+    NB = int(math.ceil(P * (pre_blocks + S) * spec.spare))
+    perm = rng.permutation(NB)
+    prompt_blocks = perm[:P * pre_blocks].reshape(P, pre_blocks)
+    free = perm[P * pre_blocks:]
+    pairs = []
+    fi = 0
+    for p in range(P):
+        for s in range(S - 1):
+            pairs.append((int(prompt_blocks[p, -1]), int(free[fi])))
+            fi += 1
+    gen = _generator(device, seed)
+    dt = DTYPES[spec.dtype]
+    k = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    v = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    return {"k_cache": k, "v_cache": v, "pairs": torch.tensor(pairs, dtype=torch.int64, device=device),
+            "prompt_len": plen, "prompt_blocks": prompt_blocks, "samples": S, "block_size": bs}
+
+
+def prefill_case(small=False, device="cpu", seed=None, prompts=None, Tq=512, prefix=1024):
+    """Chunked-prefill tile: per prompt, a ``prefix``-token paged context whose
+    last ``Tq`` tokens are the query tile (their K/V are already in the pool).
+    q: [P, Tq, Hq, D]."""
+    spec = SPECS["c5"]
+    seed = (spec.seed if seed is None else seed) + 200
+    rng = np.random.default_rng(seed)
+    P = prompts or (2 if small else 64)
+    bs = spec.bs
+    lens = np.full(P, prefix, dtype=np.int64)
+    tables, NB, _ = _tables(lens, bs, 0, spec.spare, rng)
+    dt = DTYPES[spec.dtype]
+    gen = _generator(device, seed)
+    k = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    v = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    q = _randn((P, Tq, spec.Hq, spec.D), dt, gen, device)
+    tables_t = torch.from_numpy(tables)
+    _nan_unused(k, v, tables_t, lens, bs, True)
+    return {"q": q, "k_cache": k, "v_cache": v, "block_tables": tables_t.to(device),
+            "context_lens": torch.from_numpy(lens.astype(np.int32)).to(device),
+            "scale": scale_for(spec.D), "Tq": Tq}
+
+
+def algorithmic_decode_bytes(case):
+    """HBM bytes a decode call must move at least: K and V rows of every token
+    in context, Q in, O out, the block-table entries used, the lengths."""
+    s = case.spec
+    e = case.q.element_size()
+    lens = case.context_lens.cpu().numpy().astype(np.int64)
+    kv = int(lens.sum()) * 2 * s.Hkv * s.D * e
+    qo = 2 * case.q.numel() * e
+    tbl = int(sum(-(-int(L) // s.bs) for L in lens)) * 4 + 4 * len(lens)
+    return kv + qo + tbl
+
+
+def unique_decode_bytes(case):
+    """As ``algorithmic_decode_bytes`` but counting each physical block once
+    (shared prompt blocks are read once from HBM when siblings run together)."""
+    s = case.spec
+    e = case.q.element_size()
+    lens = case.context_lens.cpu().numpy().astype(np.int64)
+    tables = case.block_tables.cpu().numpy()
+    seen = {}
+    for b, L in enumerate(lens):
+        n = -(-int(L) // s.bs)
+        for j in range(n):
+            valid = min(s.bs, int(L) - j * s.bs)
+            blk = int(tables[b, j])
+            seen[blk] = max(seen.get(blk, 0), valid)
+    kv = sum(seen.values()) * 2 * s.Hkv * s.D * e
+    qo = 2 * case.q.numel() * e
+    tbl = int(sum(-(-int(L) // s.bs) for L in lens)) * 4 + 4 * len(lens)
+    return kv + qo + tbl
+
+
+def append_bytes(case):
+    """Bytes the KV append must move: read key/value rows, write them."""
+    T = int((case.slot_mapping >= 0).sum())
+    row = case.spec.Hkv * case.spec.D * case.key.element_size()
+    return 2 * 2 * T * row + 8 * case.slot_mapping.numel()
