@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark on GB300.
+
+One step = one pass of the hot path over one batch of the bench workload:
+append each request's newest K/V (pa_reshape_and_cache) then paged decode
+attention over every request's context (pa_decode: split-K partitions and
+the log-sum-exp merge).  Default workload ``c2``: bf16 MHA, 32 heads, head_dim
+128, block_size 16, batch 64, context lengths U[128, 2048], a randomly
+permuted 1.45 GB pool (larger than the 129 MB L2, so K/V stream from HBM).
+
+Prints one JSON line.  ``value`` is HBM GB/s of algorithmic bytes (K/V rows
+of every token in context, Q, O, the block-table entries and lengths, plus
+the append's K/V rows read and written) over the device-timed K steps;
+``seq_steps_per_s`` = batch / step time.  ``--impl reference`` times the
+float64 CPU oracle on host cores on bounded samples of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "paged decode attention HBM GB/s (% of GB300 peak); seq-steps/s at batch 64"
+WORKLOAD_TEXT = {
+    "c2": "bf16 MHA decode: 32 heads, head_dim 128, block_size 16, batch 64, context U[128,2048], "
+          "scattered pool; plus reshape_and_cache of 64 new tokens",
+    "c3": "bf16 MHA decode: 40 heads, head_dim 128, block_size 16, batch 128, context log-normal "
+          "(median 512, cap 4096), scattered pool; plus reshape_and_cache of 128 new tokens",
+    "c4": "bf16 GQA decode: 32/8 heads, head_dim 128, block_size 16, batch 256, context U[1024,32768], "
+          "split-K 512; plus reshape_and_cache of 256 new tokens",
+    "c4b32": "as c4 with block_size 32",
+    "c5": "bf16 GQA decode 32/8, 64 prompts x 8 samples sharing 1024-token prompts + private tails U[0,256]; "
+          "plus reshape_and_cache of the new tokens",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel_src, workload):
+    """ncu DRAM bytes per launch of the decode kernel, from a committed
+    profile summary; None if it is missing or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", "decode_%s_traffic.json" % workload)
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return d.get("traffic_bytes_per_launch") if d.get("kernel_sha256") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"error": "no samples in the timed region"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def _widen(u16):
+    import numpy as np
+    return (u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _oracle_slice(task):
+    """One (sequence, KV head) slice through the oracle: append the newest
+    token's K/V, then decode the query heads that read this KV head."""
+    import numpy as np
+    import oracle
+    q, k, v, L, key, val, slot, scale = task
+    k, v = oracle.reshape_and_cache(_widen(key)[None], _widen(val)[None], np.array([slot]),
+                                    _widen(k), _widen(v))
+    table = np.arange(k.shape[0])[None]
+    return oracle.paged_decode(_widen(q)[None], k, v, table, np.array([L]), scale)
+
+
+def _cpu_tasks(name, nseq, seed):
+    """Oracle inputs per (sequence, KV head) slice, as bf16 bit patterns with
+    the slice's blocks gathered into a compact pool, drawn by the same
+    workload generator on the CPU.  Returns the tasks and their algorithmic
+    bytes (the same accounting as the GPU leg)."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_307_gb300 import workloads as W
+    c = W.decode_case(name, device="cpu", nan_fill=False, seed=seed, B=nseq)
+    s = c.spec
+    bs, G = s.bs, s.Hq // s.Hkv
+    lens = c.context_lens.numpy()
+    tables = c.block_tables.numpy()
+    u16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    kb, vb, qb, keyb, valb = u16(c.k_cache), u16(c.v_cache), u16(c.q), u16(c.key), u16(c.value)
+    tasks, nbytes = [], []
+    e = 2
+    for b in range(len(lens)):
+        n = -(-int(lens[b]) // bs)
+        blocks = tables[b, :n]
+        slot = int(c.slot_mapping[b])
+        local_slot = int(np.where(blocks == slot // bs)[0][0]) * bs + slot % bs
+        for g in range(s.Hkv):
+            tasks.append((qb[b, g * G:(g + 1) * G], kb[blocks][:, :, g:g + 1].copy(),
+                          vb[blocks][:, :, g:g + 1].copy(), int(lens[b]), keyb[b, g:g + 1],
+                          valb[b, g:g + 1], local_slot, c.scale))
+            nbytes.append(int(lens[b]) * 2 * s.D * e + 2 * G * s.D * e + (4 * n + 4 + 8) / s.Hkv
+                          + 2 * 2 * s.D * e)
+    return tasks, nbytes
+
+
+def _pool(cores):
+    import multiprocessing as mp
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    return mp.get_context("spawn").Pool(cores)
+
+
+def cpu_baseline(name, seconds):
+    """The oracle as it stands on (sequence, KV head) slices of a 16-sequence
+    sample, spread over the host cores (spawn pool, one BLAS thread each),
+    repeated until about `seconds` of wall time."""
+    cores = os.cpu_count() or 1
+    nseq = 16
+    tasks, nbytes = _cpu_tasks(name, nseq, seed=12345)
+    with _pool(cores) as pool:
+        pool.map(_oracle_slice, tasks[:cores])          # worker start-up outside the timing
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            pool.map(_oracle_slice, tasks, chunksize=4)
+            reps += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+    gbs = reps * sum(nbytes) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d passes over a %d-sequence sample of workload %s, split into %d (sequence, KV head) "
+                      "slices (append + decode, float64), %.1f s wall" % (reps, nseq, name, len(tasks), dt),
+            "seq_steps_per_s": round(reps * nseq / dt, 3)}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on one host core: each step is one (sequence, KV head)
+    slice of the workload (append + decode), cycling through a 16-sequence
+    sample, so K steps stay within minutes."""
+    if rank != 0:
+        return
+    tasks, nbytes = _cpu_tasks(args.workload, 16, seed=12345)
+    for i in range(args.warmup):
+        _oracle_slice(tasks[i % len(tasks)])
+    t0 = time.perf_counter()
+    done = 0.0
+    for i in range(args.steps):
+        _oracle_slice(tasks[i % len(tasks)])
+        done += nbytes[i % len(tasks)]
+    dt = time.perf_counter() - t0
+    step = dt / args.steps
+    gbs = done / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 5), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
+                   "sample": "one (sequence, KV head) slice per step"},
+        "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d (sequence, KV head) slices of a 16-sequence sample of workload %s "
+                                   "(append + decode, float64, one thread)" % (args.steps, args.workload)},
+        "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_307_gb300 import build as B
+    B.build()
+    from paged_kv_cache_307_gb300 import _lib as pa
+    from paged_kv_cache_307_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = W.SPECS[args.workload]
+    case = W.decode_case(args.workload, device=dev, nan_fill=False, seed=spec.seed + 1000 * rank)
+    Bsz, Hq, D = case.q.shape
+    ws = pa.alloc_workspace(case.q, case.k_cache, case.block_tables, args.partition)
+    out = torch.empty_like(case.q)
+    stream = torch.cuda.current_stream()
+    P = pa.partition_size(Bsz, Hq, spec.Hkv, D, case.max_blocks, spec.bs, args.partition)
+    launches_per_step = 2 + (1 if case.max_blocks * spec.bs > P else 0)
+
+    dec_bytes = W.algorithmic_decode_bytes(case)
+    app_bytes = W.append_bytes(case)
+    step_bytes = dec_bytes + app_bytes
+
+    def append():
+        pa.reshape_and_cache(case.key, case.value, case.slot_mapping, case.k_cache, case.v_cache)
+
+    def decode():
+        pa.decode(out, case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+                  case.scale, partition_size=args.partition, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        append()
+        decode()
+    torch.cuda.synchronize()
+    assert pa.last_error() == 0, "device-detected error during warm-up"
+
+    K = args.steps
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    sampler = ClockSampler(int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].isdigit()
+                           else local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    start.record(stream)
+    for i in range(K):
+        append()
+        d0[i].record(stream)
+        decode()
+        d1[i].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    dec_ms = statistics.mean(d0[i].elapsed_time(d1[i]) for i in range(K))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert pa.last_error() == 0, "device-detected error in the timed region"
+    step_s = total_ms / 1e3 / K
+    value = world * step_bytes / step_s / 1e9
+
+    # end to end through the public API: pinned host inputs in, result out
+    host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "key", "value", "slot_mapping",
+                                                             "block_tables", "context_lens")}
+    devb = {n: torch.empty_like(getattr(case, n)) for n in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for n in host:
+            devb[n].copy_(host[n], non_blocking=True)
+        pa.reshape_and_cache(devb["key"], devb["value"], devb["slot_mapping"], case.k_cache, case.v_cache)
+        pa.decode(out, devb["q"], case.k_cache, case.v_cache, devb["block_tables"], devb["context_lens"],
+                  case.scale, partition_size=args.partition, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = min(K, 1000)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    a.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * step_bytes / (e2e_ms / 1e3 / Ke) / 1e9
+
+    if rank != 0:
+        return
+    peak, peak_src = peaks()
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_307_gb300", "csrc", "pa_decode.cu"),
+                             args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
+        spec.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload], "batch": Bsz,
+                   "num_heads": Hq, "num_kv_heads": spec.Hkv, "head_dim": D, "block_size": spec.bs,
+                   "partition_tokens": P, "pool_bytes": 2 * case.k_cache.numel() * case.k_cache.element_size(),
+                   "l2": "inputs larger than L2 (K/V pool %.2f GB vs 129 MB L2); no flush"
+                         % (2 * case.k_cache.numel() * case.k_cache.element_size() / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step_bytes": step_bytes, "decode_bytes": dec_bytes, "append_bytes": app_bytes},
+        "seq_steps_per_s": round(world * Bsz / step_s, 1),
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pa_decode (decode_kernel + merge_kernel), %.4f ms per launch" % dec_ms,
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src if peak_src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": round(e2e_ms / Ke, 5)},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * pa.h — C ABI of libpa: paged KV-cache attention kernels for GB300 (sm_103a).
+ *
+ * The operations are the ones the paged-attention pages describe:
+ *
+ *   [KVS] "19.2 KV Cache 系统化管理" (paper.xwysyy.cn, llm-fullstack-book):
+ *         §19.2.2 block pool / block table, Fig 19-5 block-wise attention,
+ *         Fig 19-8 copy-on-write; §19.2.3 the simplified implementation
+ *         (pool layout, slot writes, block-table append, paged attention with
+ *         an online softmax checked against dense softmax attention).
+ *   [OS]  "LLM 推理引擎的内存管理与调度：PagedAttention、Prefix Cache 与
+ *         Continuous Batching" (zhouzhq2021.github.io): §三 the kernel looks a
+ *         logical block up in the block table and forms the physical address
+ *         and in-block offset; §四 shared blocks and copy-on-write; §8.1
+ *         chunked prefill.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pool layout (from [KVS] §19.2.3): k_cache and v_cache are each
+ *    [num_blocks, block_size, num_kv_heads, head_dim], row-major, contiguous,
+ *    one layer.  Call once per layer for a multi-layer cache.
+ *  - Element type: PA_F32 or PA_BF16; K, V, Q and the output share it.
+ *    Arithmetic is fp32 whatever the storage type; bf16 results are rounded
+ *    to nearest even.
+ *  - Supported sizes: head_dim in {32, 64, 128}; block_size in {4, 8, 16,
+ *    32}; num_heads a multiple of num_kv_heads.  Query head h reads KV head
+ *    h / (num_heads / num_kv_heads) (grouped-query attention).
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *    caller owns all memory and the library allocates nothing per call.
+ *    K/V pools, queries and outputs must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL: the legacy default stream).  Every
+ *    call only enqueues work on it and returns without synchronising.
+ *  - Return value: 0 on success, or a negative PA_ERR_* code when the host
+ *    side rejects the arguments — in that case nothing was launched.
+ *  - Conditions only the device can see (a block id outside the pool, a slot
+ *    outside the pool, a context longer than its block-table row, a
+ *    pipeline wait that ran out) never trap: the affected item is skipped or
+ *    zero-filled and a bit is OR-ed into a sticky device word that
+ *    pa_last_error() returns and clears.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* host-detected errors (negative return values) */
+#define PA_OK             0
+#define PA_ERR_NULL      (-1) /* a required pointer is NULL */
+#define PA_ERR_SHAPE     (-2) /* unsupported or inconsistent sizes */
+#define PA_ERR_DTYPE     (-3) /* unknown pa_dtype */
+#define PA_ERR_ALIGN     (-4) /* a K/V/Q/out pointer is not 16-byte aligned */
+#define PA_ERR_WORKSPACE (-5) /* workspace missing or smaller than needed */
+#define PA_ERR_CUDA      (-6) /* a CUDA runtime call failed (launch, attributes) */
+
+/* device-detected conditions (bits of pa_last_error()'s positive result) */
+#define PA_DEV_BAD_BLOCK  1u  /* block-table entry or pair id outside [0, num_blocks) */
+#define PA_DEV_BAD_SLOT   2u  /* slot_mapping entry >= num_blocks * block_size */
+#define PA_DEV_BAD_LEN    4u  /* context length < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEV_TIMEOUT    8u  /* a shared-memory pipeline wait exceeded its time limit */
+
+/*
+ * KV append ("reshape_and_cache").  [KVS] §19.2.3: a new token's key and
+ * value are written into a slot of a physical block; the slot comes from the
+ * block table (logical block = tokens so far / block_size, offset = tokens so
+ * far % block_size).  Fig 19-6: decode appends into the partly filled block.
+ *
+ *   key, value     [num_tokens, num_kv_heads, head_dim]   (read)
+ *   slot_mapping   [num_tokens] int64: physical_block * block_size + offset.
+ *                  A negative slot is padding and is skipped.  Slots must be
+ *                  distinct within one call (duplicates: unspecified winner).
+ *   k_cache, v_cache  pool (written only at the addressed slots)
+ *
+ * Exact byte copy.  A slot >= num_blocks * block_size is skipped and sets
+ * PA_DEV_BAD_SLOT.  num_tokens == 0 launches nothing.
+ */
+int pa_reshape_and_cache(const void* key, const void* value,
+                         const int64_t* slot_mapping, int num_tokens,
+                         void* k_cache, void* v_cache,
+                         int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         pa_dtype dtype, void* stream);
+
+/*
+ * Paged decode attention.  [KVS] §19.2.3 / Fig 19-5 and [OS] §三: for each
+ * sequence b and query head h (KV head g = h / (num_heads/num_kv_heads)),
+ *
+ *   out[b,h,:] = sum_{t < L_b} softmax_t(scale * <q[b,h,:], K_b[t,g,:]>) V_b[t,g,:]
+ *
+ * where token t of sequence b sits in physical block
+ * block_tables[b*max_blocks_per_seq + t/block_size] at slot t % block_size,
+ * and L_b = context_lens[b] counts the newest token (append it first).
+ * Only the valid slots of the last block are read; L_b == 0 gives zeros.
+ *
+ *   out            [num_seqs, num_heads, head_dim]        (written)
+ *   query          [num_seqs, num_heads, head_dim]
+ *   block_tables   [num_seqs, max_blocks_per_seq] int32
+ *   context_lens   [num_seqs] int32
+ *   scale          the pages use 1/sqrt(head_dim)
+ *   partition_size split-K partition in tokens: 0 = automatic, < 0 = never
+ *                  split, > 0 = a multiple of block_size.  A sequence longer
+ *                  than one partition is processed as independent partitions
+ *                  whose (max, sum, unnormalised output) states are merged by
+ *                  log-sum-exp in a second kernel.
+ *   workspace      device scratch of at least pa_decode_workspace_bytes()
+ *                  with the same sizes (may be NULL when that is 0).  Its
+ *                  contents on entry do not matter; calls that share one
+ *                  workspace must be ordered (same stream).
+ *
+ * Output is fp32-accumulated; bf16 output is rounded to nearest even.
+ */
+int pa_decode(void* out, const void* query,
+              const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int num_seqs,
+              int num_heads, int num_kv_heads, int head_dim,
+              int block_size, int num_blocks, float scale, int partition_size,
+              void* workspace, size_t workspace_bytes,
+              pa_dtype dtype, void* stream);
+
+/* Bytes of workspace pa_decode needs for these sizes (0 when no sequence can
+ * span more than one partition).  Pure host arithmetic; no CUDA call. */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_size);
+
+/* The partition size (tokens) pa_decode will use for these arguments. */
+int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                             int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * Copy-on-write block copy.  [KVS] Fig 19-8 and [OS] §四: before a sequence
+ * writes into a block that other sequences still share, a new block is
+ * allocated and the old contents are copied into it.  For each pair i,
+ * block pairs[2i+1] of both k_cache and v_cache becomes a byte-exact copy of
+ * block pairs[2i] (all block_size slots, all heads).
+ *
+ *   pairs   [num_pairs, 2] int64 (src, dst), device memory.  dsts must be
+ *           distinct and no dst may be the src of another pair.
+ *
+ * A pair with an id outside [0, num_blocks) is skipped and sets
+ * PA_DEV_BAD_BLOCK.  num_pairs == 0 launches nothing.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
+                   int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                   pa_dtype dtype, void* stream);
+
+/* Return the sticky device-detected condition bits (PA_DEV_*) and clear
+ * them.  Synchronises the current device; 0 means nothing was detected.
+ * Returns PA_ERR_CUDA if the device cannot be read. */
+int pa_last_error(void);
+
+/* Human-readable text for a PA_ERR_* code or a PA_DEV_* bit. */
+const char* pa_strerror(int code);
+
+/* Library ABI version (major*100 + minor). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,145 @@
+"""ctypes binding to libpa.so: argument marshalling only.
+
+Every step of the path runs in libpa's CUDA kernels; this module turns torch
+tensors into raw device pointers and sizes, passes torch's current CUDA
+stream, and raises on a non-zero return.  There is no fallback: if libpa.so
+is missing the import of this module fails.
+"""
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "pa.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libpa.so is not built (run paged_kv_cache_307_gb300.build.build()): " + LIB_PATH)
+
+lib = ctypes.CDLL(LIB_PATH)
+
+PA_F32, PA_BF16 = 0, 1
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
+
+_p, _i, _f, _sz, _i64p, _i32p = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                                 ctypes.c_void_p, ctypes.c_void_p)
+
+lib.pa_reshape_and_cache.argtypes = [_p, _p, _i64p, _i, _p, _p, _i, _i, _i, _i, _i, _p]
+lib.pa_reshape_and_cache.restype = _i
+lib.pa_decode.argtypes = [_p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _i, _p]
+lib.pa_decode.restype = _i
+lib.pa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+lib.pa_decode_workspace_bytes.restype = _sz
+lib.pa_decode_partition_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+lib.pa_decode_partition_size.restype = _i
+lib.pa_copy_blocks.argtypes = [_p, _p, _i64p, _i, _i, _i, _i, _i, _i, _p]
+lib.pa_copy_blocks.restype = _i
+lib.pa_last_error.argtypes = []
+lib.pa_last_error.restype = _i
+lib.pa_strerror.argtypes = [_i]
+lib.pa_strerror.restype = ctypes.c_char_p
+lib.pa_version.argtypes = []
+lib.pa_version.restype = _i
+
+
+class PAError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__("%s failed: %s (%d)" % (what, lib.pa_strerror(code).decode(), code))
+        self.code = code
+
+
+def declared_functions():
+    """Names of the functions include/pa.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+
+
+def _dtype(t):
+    if t.dtype == torch.float32:
+        return PA_F32
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code, what):
+    if code != 0:
+        raise PAError(code, what)
+
+
+def _contig(*ts):
+    for t in ts:
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def reshape_and_cache(key, value, slot_mapping, k_cache, v_cache, stream=None):
+    """Append key/value [T, Hkv, D] into the pool slots named by slot_mapping."""
+    _contig(key, value, slot_mapping, k_cache, v_cache)
+    NB, bs, H, D = k_cache.shape
+    assert slot_mapping.dtype == torch.int64
+    _check(lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
+                                    _ptr(k_cache), _ptr(v_cache), NB, bs, H, D, _dtype(k_cache),
+                                    _stream(stream)), "pa_reshape_and_cache")
+
+
+def workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, partition_size=0):
+    return lib.pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
+                                         block_size, partition_size)
+
+
+def partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, partition_size=0):
+    return lib.pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
+                                        block_size, partition_size)
+
+
+def alloc_workspace(q, k_cache, block_tables, partition_size=0):
+    B, Hq, D = q.shape
+    n = workspace_bytes(B, Hq, k_cache.shape[2], D, block_tables.shape[1], k_cache.shape[1], partition_size)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+
+
+def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, partition_size=0,
+           workspace=None, stream=None):
+    """out[B,Hq,D] = paged decode attention of q[B,Hq,D] over the pool."""
+    _contig(out, q, k_cache, v_cache, block_tables, context_lens)
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if workspace is None:
+        workspace = alloc_workspace(q, k_cache, block_tables, partition_size)
+    _check(lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                         block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
+                         ctypes.c_float(scale), partition_size, _ptr(workspace), workspace.numel(),
+                         _dtype(q), _stream(stream)), "pa_decode")
+    return out
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """Copy-on-write: block pairs[i,1] becomes a copy of block pairs[i,0]."""
+    _contig(k_cache, v_cache, pairs)
+    assert pairs.dtype == torch.int64
+    NB, bs, H, D = k_cache.shape
+    _check(lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], NB, bs, H, D,
+                              _dtype(k_cache), _stream(stream)), "pa_copy_blocks")
+
+
+def last_error():
+    """Sticky device-detected condition bits (and clear them); synchronises."""
+    code = lib.pa_last_error()
+    if code < 0:
+        raise PAError(code, "pa_last_error")
+    return code

@@ -1,0 +1,84 @@
+// pa_api.cu — library-wide entry points: status word, error text, version,
+// and the host helpers shared by the kernels (SM count, TMA tensor maps).
+#include "pa_common.cuh"
+
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace pa {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int num_blocks, int block_size,
+                     int num_kv_heads, int head_dim) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t e = (cuuint64_t)elem_bytes(dt);
+  // innermost first: head_dim, kv head, slot in block, block
+  cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+                        (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {head_dim * e, (cuuint64_t)num_kv_heads * head_dim * e,
+                           (cuuint64_t)block_size * num_kv_heads * head_dim * e};
+  cuuint32_t box[4] = {(cuuint32_t)head_dim, 1, (cuuint32_t)block_size, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, dt == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace pa
+
+extern "C" int pa_last_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  const unsigned a = pa::fetch_status_cache_ops();
+  const unsigned b = pa::fetch_status_decode();
+  if (a == 0xffffffffu || b == 0xffffffffu) return PA_ERR_CUDA;
+  return (int)(a | b);
+}
+
+extern "C" const char* pa_strerror(int code) {
+  switch (code) {
+    case PA_OK: return "success";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case PA_ERR_DTYPE: return "unknown element type";
+    case PA_ERR_ALIGN: return "a K/V/Q/output pointer is not 16-byte aligned";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "a CUDA runtime call failed";
+    case (int)PA_DEV_BAD_BLOCK: return "device: block id outside the pool";
+    case (int)PA_DEV_BAD_SLOT: return "device: slot outside the pool";
+    case (int)PA_DEV_BAD_LEN: return "device: context length outside its block-table row";
+    case (int)PA_DEV_TIMEOUT: return "device: pipeline wait timed out";
+    default: return code > 0 ? "device: several conditions (bitmask)" : "unknown error";
+  }
+}
+
+extern "C" int pa_version(void) { return 100; }

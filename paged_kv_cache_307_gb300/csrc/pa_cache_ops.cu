@@ -1,0 +1,126 @@
+// pa_cache_ops.cu — KV append (reshape_and_cache) and copy-on-write block copy.
+//
+// Both are pure data movement, bound by HBM bandwidth, and must be byte-exact:
+//  * append: "19.2 KV Cache 系统化管理" §19.2.3 (a token's K/V written into a
+//    slot of a physical block; slot from the block-table append) and Fig 19-6
+//    (decode appends into the partly filled last block);
+//  * copy: the same page's Fig 19-8 (copy-on-write: a new block receives the
+//    old block's contents before the table is remapped) and "LLM 推理引擎的
+//    内存管理与调度…" §四.
+//
+// Layout: each token's K (or V) row for all heads, [Hkv, D], is contiguous in
+// both the source [T, Hkv, D] and the pool [NB, bs, Hkv, D]; a whole block is
+// contiguous too.  So both kernels are 16-byte vector copies of contiguous
+// spans: one CTA per (token, K|V) for the append, one CTA per (pair, K|V,
+// span) for the block copy.  Loads use the non-coherent path with no L1
+// allocation (each byte is read once); several 16-byte loads are in flight
+// per thread before the stores.
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_status_cache;
+
+constexpr int kCopyThreads = 256;
+constexpr int kUnroll = 4;
+
+// Copy `chunks` 16-byte chunks from src to dst with the whole CTA.
+__device__ __forceinline__ void cta_copy16(unsigned char* __restrict__ dst,
+                                           const unsigned char* __restrict__ src, int chunks) {
+  int c = threadIdx.x;
+  for (; c + (kUnroll - 1) * kCopyThreads < chunks; c += kUnroll * kCopyThreads) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = ld_nc_v4(src + (size_t)(c + u * kCopyThreads) * 16);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) st_v4(dst + (size_t)(c + u * kCopyThreads) * 16, v[u]);
+  }
+  for (; c < chunks; c += kCopyThreads) st_v4(dst + (size_t)c * 16, ld_nc_v4(src + (size_t)c * 16));
+}
+
+// grid: (num_tokens, 2).  blockIdx.y selects K (0) or V (1).
+__global__ void __launch_bounds__(kCopyThreads)
+reshape_and_cache_kernel(const unsigned char* __restrict__ key, const unsigned char* __restrict__ value,
+                         const int64_t* __restrict__ slot_mapping,
+                         unsigned char* __restrict__ k_cache, unsigned char* __restrict__ v_cache,
+                         long long num_slots, int row_bytes) {
+  const int t = blockIdx.x;
+  const long long slot = slot_mapping[t];
+  if (slot < 0) return;                       // padding
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_status_cache, PA_DEV_BAD_SLOT);
+    return;
+  }
+  const unsigned char* src = (blockIdx.y == 0 ? key : value) + (size_t)t * row_bytes;
+  unsigned char* dst = (blockIdx.y == 0 ? k_cache : v_cache) + (size_t)slot * row_bytes;
+  cta_copy16(dst, src, row_bytes / 16);
+}
+
+// grid: (num_pairs, 2, spans).  Each CTA copies one span of one block.
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(unsigned char* __restrict__ k_cache, unsigned char* __restrict__ v_cache,
+                   const int64_t* __restrict__ pairs, long long num_blocks,
+                   long long block_bytes, int span_bytes) {
+  const long long src = pairs[2 * (size_t)blockIdx.x];
+  const long long dst = pairs[2 * (size_t)blockIdx.x + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(&g_status_cache, PA_DEV_BAD_BLOCK);
+    return;
+  }
+  unsigned char* base = blockIdx.y == 0 ? k_cache : v_cache;
+  const long long off = (long long)blockIdx.z * span_bytes;
+  const long long n = block_bytes - off < span_bytes ? block_bytes - off : span_bytes;
+  cta_copy16(base + dst * block_bytes + off, base + src * block_bytes + off, (int)(n / 16));
+}
+
+}  // namespace
+
+unsigned fetch_status_cache_ops() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_cache, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (v && cudaMemcpyToSymbol(g_status_cache, &zero, sizeof(zero)) != cudaSuccess) return 0xffffffffu;
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_reshape_and_cache(const void* key, const void* value, const int64_t* slot_mapping,
+                                    int num_tokens, void* k_cache, void* v_cache, int num_blocks,
+                                    int block_size, int num_kv_heads, int head_dim, pa_dtype dtype,
+                                    void* stream) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || !supported_head_dim(head_dim) ||
+      !supported_block_size(block_size))
+    return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !k_cache || !v_cache) return PA_ERR_NULL;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  const int row_bytes = num_kv_heads * head_dim * elem_bytes(dtype);
+  dim3 grid((unsigned)num_tokens, 2);
+  reshape_and_cache_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
+      (const unsigned char*)key, (const unsigned char*)value, slot_mapping, (unsigned char*)k_cache,
+      (unsigned char*)v_cache, (long long)num_blocks * block_size, row_bytes);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
+                              int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                              pa_dtype dtype, void* stream) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || !supported_head_dim(head_dim) ||
+      !supported_block_size(block_size))
+    return PA_ERR_SHAPE;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !pairs) return PA_ERR_NULL;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  const long long block_bytes = (long long)block_size * num_kv_heads * head_dim * elem_bytes(dtype);
+  const int span = 32 * 1024;
+  const unsigned spans = (unsigned)((block_bytes + span - 1) / span);
+  dim3 grid((unsigned)num_pairs, 2, spans);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
+      (unsigned char*)k_cache, (unsigned char*)v_cache, pairs, num_blocks, block_bytes, span);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

@@ -1,0 +1,601 @@
+// pa_decode.cu — paged decode attention (GQA, split-K) and its merge kernel.
+//
+// What it computes ("19.2 KV Cache 系统化管理" §19.2.3 and Fig 19-5; "LLM 推理
+// 引擎的内存管理与调度…" §三): for each sequence b and query head h, attention of
+// q[b,h] over the sequence's K/V, which sit in fixed-size physical blocks named
+// by the block table; only the valid slots of the last block count; the
+// softmax is accumulated block by block with a running maximum, a running sum
+// of exponentials and a rescaled output, normalised at the end.
+//
+// How (GB300):
+//  * Work item = (sequence, KV head, query-head subgroup, partition of P
+//    tokens).  A persistent grid (resident CTAs x SMs) strides over the item
+//    space; the sequence index is innermost so CTAs running side by side read
+//    the same blocks when sequences share a prompt.
+//  * Each CTA = 1 producer warp + kConsumerWarps consumer warps.  The producer
+//    reads the item's block-table entries with one coalesced warp load, then
+//    issues, per block, two TMA tensor loads (box {D, 1 head, bs, 1 block} of
+//    the [NB, bs, Hkv, D] pool) for K and V into a ring of shared-memory
+//    stages, completing on an mbarrier with transaction bytes.  A block id
+//    outside the pool is flagged and replaced by block 0, so no copy leaves
+//    the pool.
+//  * Consumer warps take the item's blocks round-robin.  Inside a warp, LPT
+//    lanes share one token (each lane owns two 16-byte chunks of head_dim), so
+//    one warp covers TPW tokens per pass with conflict-free 16-byte shared
+//    loads.  Each lane group keeps its own online-softmax state (m, l, o) for
+//    its tokens; group, warp and partition states are merged by log-sum-exp at
+//    the end, which is exact up to rounding (the update is associative).
+//  * Scores are computed in the base-2 domain (q pre-multiplied by
+//    scale*log2 e), with exp2f.  The K/V rows are read once from HBM and used
+//    for all GT query heads of the subgroup (GQA) straight from registers.
+//  * A sequence whose context fits one partition is normalised and written
+//    directly; longer ones write (m, l, unnormalised o) per partition to the
+//    workspace, and merge_kernel combines them.
+//  * Waits are bounded (2 s).  A wait that runs out sets PA_DEV_TIMEOUT and an
+//    abort flag; every role then skips the remaining work while still passing
+//    the CTA's barriers, and the producer waits (bounded) for the TMA loads it
+//    issued before the CTA exits.
+#include "pa_common.cuh"
+
+#include <mutex>
+#include <map>
+#include <tuple>
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_status_decode;
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_ml;       // [B*Hq*max_parts][2]   (m in log2 units, l)
+  float* ws_o;        // [B*Hq*max_parts][D]   unnormalised output
+  int B, Hq, Hkv, G, nsub;
+  int max_blocks, bs, num_blocks;
+  int part_tokens, max_parts;
+  long long n_virtual;
+  float qscale;       // scale * log2(e)
+  int stages;
+  uint32_t tile_bytes;
+};
+
+struct Item {
+  int b, kvh, sg, part, t1, jb, je;
+  bool split;
+};
+
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, Item& it) {
+  it.b = (int)(v % p.B);
+  long long r = v / p.B;
+  it.kvh = (int)(r % p.Hkv);
+  r /= p.Hkv;
+  it.sg = (int)(r % p.nsub);
+  it.part = (int)(r / p.nsub);
+  int L = __ldg(&p.context_lens[it.b]);
+  const int Lmax = p.max_blocks * p.bs;
+  if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;   // flagged by the consumer
+  const int nparts = L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+  if (it.part >= nparts) return false;
+  const int t0 = it.part * p.part_tokens;
+  it.t1 = min(L, t0 + p.part_tokens);
+  it.jb = t0 / p.bs;
+  it.je = (it.t1 + p.bs - 1) / p.bs;
+  if (it.je < it.jb) it.je = it.jb;
+  it.split = nparts > 1;
+  return true;
+}
+
+template <typename T, int D, int GT>
+__global__ void __launch_bounds__(kThreads)
+decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+              const DecodeParams p) {
+  using E = Elem<T>;
+  constexpr int CHUNKS = D * E::kBytes / 16;   // 16-byte chunks per token row
+  constexpr int LPT = CHUNKS / 2;              // lanes per token
+  constexpr int TPW = 32 / LPT;                // tokens per warp pass
+  constexpr int EPC = E::kPerChunk;            // elements per chunk
+  constexpr int DPL = 2 * EPC;                 // head dims per lane
+  constexpr int NS = TPW >= 16 ? 1 : 16 / TPW; // tokens per lane group per softmax step
+  constexpr int ROW = D * E::kBytes;
+  constexpr int NCW = kConsumerWarps;
+  static_assert(LPT >= 1 && LPT <= 32 && (32 % LPT) == 0, "lane split");
+
+  const int S = p.stages;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* tilesK = smem;
+  unsigned char* tilesV = smem + (size_t)S * p.tile_bytes;
+  float* mbuf = reinterpret_cast<float*>(tilesV + (size_t)S * p.tile_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + NCW * GT * (D + 2));
+  uint64_t* empty = full + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  uint32_t it = 0;  // position in this CTA's block stream, identical in every role
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&mapK);
+      prefetch_tensormap(&mapV);
+    }
+    const uint64_t pol = policy_evict_first();
+    uint32_t issued = 0;
+    for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
+      Item item;
+      if (!decode_item(p, v, item)) continue;
+      const int32_t* row = p.block_tables + (size_t)item.b * p.max_blocks;
+      for (int j0 = item.jb; j0 < item.je; j0 += 32) {
+        const int n = min(32, item.je - j0);
+        int blk = 0;
+        if (lane < n) {
+          blk = __ldg(&row[j0 + lane]);
+          if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            atomicOr(&g_status_decode, PA_DEV_BAD_BLOCK);
+            blk = 0;    // keep every copy inside the pool
+          }
+        }
+        for (int i = 0; i < n; ++i) {
+          const int bi = __shfl_sync(0xffffffffu, blk, i);
+          if (lane == 0 && !*abort_flag) {
+            const int st = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(&empty[st], ph ^ 1u)) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            } else {
+              mbar_arrive_expect_tx(&full[st], 2u * p.tile_bytes);
+              tma_load_4d(tilesK + (size_t)st * p.tile_bytes, &mapK, &full[st], 0, item.kvh, 0, bi, pol);
+              tma_load_4d(tilesV + (size_t)st * p.tile_bytes, &mapV, &full[st], 0, item.kvh, 0, bi, pol);
+              issued = it + 1;
+            }
+          }
+          ++it;
+        }
+      }
+    }
+    // Never leave the CTA with TMA writes into its shared memory in flight.
+    if (lane == 0) {
+      const uint32_t first = issued > (uint32_t)S ? issued - S : 0u;
+      for (uint32_t k = first; k < issued; ++k) mbar_wait(&full[k % S], (k / S) & 1u);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int grp = lane / LPT;     // token slot within a warp pass
+  const int li = lane % LPT;      // chunk owner within the token row
+  const int c0 = li, c1 = li + LPT;
+  const int ctid = threadIdx.x;   // 0 .. NCW*32-1
+
+  for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
+    Item item;
+    if (!decode_item(p, v, item)) continue;
+    if (ctid == 0 && item.kvh == 0 && item.sg == 0 && item.part == 0) {
+      const int L = __ldg(&p.context_lens[item.b]);
+      if (L < 0 || L > p.max_blocks * p.bs) atomicOr(&g_status_decode, PA_DEV_BAD_LEN);
+    }
+    const int h0 = item.kvh * p.G + item.sg * GT;
+
+    float q[GT][DPL];
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      const unsigned char* qrow =
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + h) * ROW;
+      float f[EPC];
+      E::unpack(__ldg(reinterpret_cast<const uint4*>(qrow + c0 * 16)), f);
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) q[h][e] = f[e] * p.qscale;
+      E::unpack(__ldg(reinterpret_cast<const uint4*>(qrow + c1 * 16)), f);
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) q[h][EPC + e] = f[e] * p.qscale;
+    }
+    float m[GT], l[GT], o[GT][DPL];
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
+    }
+
+    const int nblk = item.je - item.jb;
+    for (int i = 0; i < nblk; ++i, ++it) {
+      if (i % NCW != warp) continue;
+      const int st = it % S;
+      const uint32_t ph = (it / S) & 1u;
+      bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+      if (live) {
+        const bool late = !mbar_wait(&full[st], ph);
+        if (__any_sync(0xffffffffu, late)) {
+          live = false;
+          if (lane == 0) {
+            atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+        }
+      }
+      if (live) {
+        const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
+        const unsigned char* kt = tilesK + (size_t)st * p.tile_bytes;
+        const unsigned char* vt = tilesV + (size_t)st * p.tile_bytes;
+        for (int tb = 0; tb < valid; tb += TPW * NS) {
+          float s[NS][GT];
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            const int t = tb + k * TPW + grp;
+            const bool ok = t < valid;
+            float part[GT];
+#pragma unroll
+            for (int h = 0; h < GT; ++h) part[h] = 0.f;
+            if (ok) {
+              float kf[DPL];
+              E::unpack(*reinterpret_cast<const uint4*>(kt + t * ROW + c0 * 16), kf);
+              E::unpack(*reinterpret_cast<const uint4*>(kt + t * ROW + c1 * 16), kf + EPC);
+#pragma unroll
+              for (int h = 0; h < GT; ++h)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) part[h] = fmaf(q[h][d], kf[d], part[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < GT; ++h) {
+#pragma unroll
+              for (int off = LPT / 2; off > 0; off >>= 1)
+                part[h] += __shfl_xor_sync(0xffffffffu, part[h], off);
+              s[k][h] = ok ? part[h] : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < GT; ++h) {
+            float mx = m[h];
+#pragma unroll
+            for (int k = 0; k < NS; ++k) mx = fmaxf(mx, s[k][h]);
+            const float alpha = mx == -INFINITY ? 1.f : exp2f(m[h] - mx);
+            m[h] = mx;
+            l[h] *= alpha;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) o[h][d] *= alpha;
+          }
+#pragma unroll
+          for (int k = 0; k < NS; ++k) {
+            const int t = tb + k * TPW + grp;
+            if (t < valid) {
+              float vf[DPL];
+              E::unpack(*reinterpret_cast<const uint4*>(vt + t * ROW + c0 * 16), vf);
+              E::unpack(*reinterpret_cast<const uint4*>(vt + t * ROW + c1 * 16), vf + EPC);
+#pragma unroll
+              for (int h = 0; h < GT; ++h) {
+                const float pk = exp2f(s[k][h] - m[h]);
+                l[h] += pk;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(pk, vf[d], o[h][d]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // merge the lane groups of this warp (lanes with equal li own equal dims)
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m[h], off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l[h], off);
+        const float M = fmaxf(m[h], m2);
+        const float a = m[h] == -INFINITY ? 0.f : exp2f(m[h] - M);
+        const float b = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
+        l[h] = a * l[h] + b * l2;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) {
+          const float o2 = __shfl_xor_sync(0xffffffffu, o[h][d], off);
+          o[h][d] = a * o[h][d] + b * o2;
+        }
+        m[h] = M;
+      }
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        float* dst = mbuf + (warp * GT + h) * (D + 2);
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) {
+          dst[c0 * EPC + e] = o[h][e];
+          dst[c1 * EPC + e] = o[h][EPC + e];
+        }
+        if (li == 0) {
+          dst[D] = m[h];
+          dst[D + 1] = l[h];
+        }
+      }
+    }
+    named_sync(1, NCW * 32);
+
+    // merge the warps and write this item's result
+    for (int idx = ctid; idx < GT * D; idx += NCW * 32) {
+      const int h = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, mbuf[(w * GT + h) * (D + 2) + D]);
+      float num = 0.f, den = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float* src = mbuf + (w * GT + h) * (D + 2);
+          const float a = src[D] == -INFINITY ? 0.f : exp2f(src[D] - M);
+          num = fmaf(a, src[d], num);
+          den = fmaf(a, src[D + 1], den);
+        }
+      }
+      const size_t bh = (size_t)item.b * p.Hq + h0 + h;
+      if (!item.split) {
+        E::store1(static_cast<T*>(p.out) + bh * D + d, den > 0.f ? num / den : 0.f);
+      } else {
+        const size_t slot = bh * p.max_parts + item.part;
+        p.ws_o[slot * D + d] = num;
+        if (d == 0) {
+          p.ws_ml[slot * 2] = M;
+          p.ws_ml[slot * 2 + 1] = den;
+        }
+      }
+    }
+    named_sync(1, NCW * 32);
+  }
+}
+
+// One warp per (sequence, query head) with more than one partition.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+merge_kernel(const DecodeParams p) {
+  using E = Elem<T>;
+  constexpr int PER = D / 32;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)p.B * p.Hq) return;
+  const int b = (int)(gw / p.Hq);
+  int L = __ldg(&p.context_lens[b]);
+  const int Lmax = p.max_blocks * p.bs;
+  if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;
+  const int nparts = L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+  if (nparts <= 1) return;
+  const size_t base = (size_t)gw * p.max_parts;
+  float M = -INFINITY;
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[(base + i) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float den = 0.f;
+  for (int i = lane; i < nparts; i += 32) {
+    const float mi = p.ws_ml[(base + i) * 2];
+    if (mi != -INFINITY) den += exp2f(mi - M) * p.ws_ml[(base + i) * 2 + 1];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  for (int i = 0; i < nparts; ++i) {
+    const float mi = p.ws_ml[(base + i) * 2];
+    const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
+    const float* oi = p.ws_o + (base + i) * D;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oi[lane + 32 * k], acc[k]);
+  }
+  T* out = static_cast<T*>(p.out) + (size_t)gw * D;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) E::store1(out + lane + 32 * k, den > 0.f ? acc[k] / den : 0.f);
+}
+
+// ------------------------------------------------------------------ host side
+
+struct Launch {
+  const void* kernel;
+  const void* merge;
+};
+
+template <typename T, int D, int GT>
+Launch pick3() {
+  return {reinterpret_cast<const void*>(&decode_kernel<T, D, GT>),
+          reinterpret_cast<const void*>(&merge_kernel<T, D>)};
+}
+
+template <typename T, int D>
+Launch pick2(int gt) {
+  if (gt == 4) return pick3<T, D, 4>();
+  if (gt == 2) return pick3<T, D, 2>();
+  return pick3<T, D, 1>();
+}
+
+template <typename T>
+Launch pick1(int d, int gt) {
+  if (d == 32) return pick2<T, 32>(gt);
+  if (d == 64) return pick2<T, 64>(gt);
+  return pick2<T, 128>(gt);
+}
+
+struct KernelInfo {
+  int occupancy = 0;
+};
+
+std::mutex g_mu;
+std::map<std::tuple<const void*, int, size_t>, KernelInfo> g_kinfo;  // (kernel, device, smem)
+
+struct MapKey {
+  const void* base;
+  int dt, nb, bs, h, d, dev;
+  bool operator<(const MapKey& o) const {
+    return std::tie(base, dt, nb, bs, h, d, dev) < std::tie(o.base, o.dt, o.nb, o.bs, o.h, o.d, o.dev);
+  }
+};
+std::map<MapKey, CUtensorMap> g_maps;
+
+bool get_map(CUtensorMap* out, const void* base, pa_dtype dt, int nb, int bs, int h, int d, int dev) {
+  MapKey key{base, (int)dt, nb, bs, h, d, dev};
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto f = g_maps.find(key);
+  if (f != g_maps.end()) {
+    *out = f->second;
+    return true;
+  }
+  if (!encode_pool_map(out, base, dt, nb, bs, h, d)) return false;
+  if (g_maps.size() > 64) g_maps.clear();
+  g_maps[key] = *out;
+  return true;
+}
+
+int occupancy_for(const void* kernel, size_t smem, int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(kernel, dev, smem);
+  auto f = g_kinfo.find(key);
+  if (f != g_kinfo.end()) return f->second.occupancy;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem) != cudaSuccess) return 0;
+  g_kinfo[key] = KernelInfo{occ};
+  return occ;
+}
+
+int resolve_partition(int max_blocks, int bs, int partition_size) {
+  const int max_ctx = max_blocks * bs;
+  if (partition_size < 0) return max_ctx;
+  int P = partition_size > 0 ? partition_size : 512;
+  if (P >= max_ctx) P = max_ctx;
+  return P;
+}
+
+}  // namespace
+
+unsigned fetch_status_decode() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_decode, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (v && cudaMemcpyToSymbol(g_status_decode, &zero, sizeof(zero)) != cudaSuccess) return 0xffffffffu;
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int block_size, int partition_size) {
+  (void)num_seqs; (void)num_heads; (void)num_kv_heads; (void)head_dim;
+  if (max_blocks_per_seq <= 0 || !supported_block_size(block_size)) return PA_ERR_SHAPE;
+  if (partition_size > 0 && partition_size % block_size) return PA_ERR_SHAPE;
+  return resolve_partition(max_blocks_per_seq, block_size, partition_size);
+}
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                           int max_blocks_per_seq, int block_size, int partition_size) {
+  const int P = pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                         block_size, partition_size);
+  if (P <= 0 || num_seqs <= 0 || num_heads <= 0) return 0;
+  const long long max_ctx = (long long)max_blocks_per_seq * block_size;
+  const long long max_parts = (max_ctx + P - 1) / P;
+  if (max_parts <= 1) return 0;
+  const long long rows = (long long)num_seqs * num_heads * max_parts;
+  const long long ml = ((rows * 2 * 4) + 255) / 256 * 256;
+  return (size_t)(ml + rows * head_dim * 4);
+}
+
+extern "C" int pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                         int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, float scale, int partition_size, void* workspace,
+                         size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+      !supported_head_dim(head_dim) || !supported_block_size(block_size) || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PA_ERR_SHAPE;
+  if (partition_size > 0 && partition_size % block_size) return PA_ERR_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+
+  const int P = resolve_partition(max_blocks_per_seq, block_size, partition_size);
+  const long long max_ctx = (long long)max_blocks_per_seq * block_size;
+  const int max_parts = (int)((max_ctx + P - 1) / P);
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                max_blocks_per_seq, block_size, partition_size);
+  if (need && (!workspace || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  CUtensorMap mapK, mapV;
+  if (!get_map(&mapK, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev) ||
+      !get_map(&mapV, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev))
+    return PA_ERR_CUDA;
+
+  const int G = num_heads / num_kv_heads;
+  const int GT = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+
+  DecodeParams prm;
+  prm.out = out;
+  prm.q = query;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  const long long rows = (long long)num_seqs * num_heads * max_parts;
+  prm.ws_ml = need ? static_cast<float*>(workspace) : nullptr;
+  prm.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * 8) + 255) / 256 * 256)
+                  : nullptr;
+  prm.B = num_seqs;
+  prm.Hq = num_heads;
+  prm.Hkv = num_kv_heads;
+  prm.G = G;
+  prm.nsub = G / GT;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.bs = block_size;
+  prm.num_blocks = num_blocks;
+  prm.part_tokens = P;
+  prm.max_parts = max_parts;
+  prm.n_virtual = (long long)max_parts * prm.nsub * num_kv_heads * num_seqs;
+  prm.qscale = scale * kLog2e;
+  prm.tile_bytes = (uint32_t)(block_size * head_dim * elem_bytes(dtype));
+  // ~48 KB of K/V stages per CTA, at least 2.
+  int S = (int)(49152 / (2 * prm.tile_bytes));
+  S = S < 2 ? 2 : (S > 8 ? 8 : S);
+  prm.stages = S;
+
+  const Launch L = dtype == PA_F32 ? pick1<float>(head_dim, GT) : pick1<__nv_bfloat16>(head_dim, GT);
+  const size_t smem = 2 * (size_t)S * prm.tile_bytes +
+                      (size_t)kConsumerWarps * GT * (head_dim + 2) * sizeof(float) +
+                      2 * (size_t)S * sizeof(uint64_t) + 16;
+  const int occ = occupancy_for(L.kernel, smem, dev);
+  if (occ <= 0) return PA_ERR_CUDA;
+  long long grid = (long long)occ * device_sm_count();
+  if (grid > prm.n_virtual) grid = prm.n_virtual;
+
+  void* args[] = {&mapK, &mapV, &prm};
+  if (cudaLaunchKernel(L.kernel, dim3((unsigned)grid), dim3(kThreads), args, smem, (cudaStream_t)stream) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  if (max_parts > 1) {
+    const long long warps = (long long)num_seqs * num_heads;
+    const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+    void* margs[] = {&prm};
+    if (cudaLaunchKernel(L.merge, dim3(blocks), dim3(256), margs, 0, (cudaStream_t)stream) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}

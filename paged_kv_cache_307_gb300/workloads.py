@@ -163,15 +163,18 @@ def _tables(lens, bs, NB_min, spare, rng, fixed_pool=0):
     return tables, NB, perm[off:]
 
 
-def decode_case(name, small=False, device="cpu", nan_fill=True, seed=None, B=None):
+def decode_case(name, small=False, device="cpu", nan_fill=True, seed=None, B=None, lens=None):
     """Build one decode workload.  The pool holds every token of every context
     except each sequence's newest one (position L-1), whose K/V arrive in
     ``key``/``value`` with its slot in ``slot_mapping``: the caller appends,
-    then attends (context_lens count the newest token)."""
+    then attends (context_lens count the newest token).  ``lens`` overrides
+    the drawn context lengths (and the batch size)."""
     spec = SPECS[name]
     seed = spec.seed if seed is None else seed
     rng = np.random.default_rng(seed)
-    if B is None:
+    if lens is not None:
+        B = len(lens)
+    elif B is None:
         B = SMALL_B[name] if small else spec.B
     dt = DTYPES[spec.dtype]
     gen = _generator(device, seed)
@@ -180,7 +183,7 @@ def decode_case(name, small=False, device="cpu", nan_fill=True, seed=None, B=Non
     if spec.lens[0] == "shared":
         return _shared_prefix_case(spec, B, rng, gen, device, nan_fill)
 
-    lens = _lengths(spec, B, rng)
+    lens = _lengths(spec, B, rng) if lens is None else np.asarray(lens, dtype=np.int64)
     max_len = spec.lens[1] if spec.lens[0] == "fixed" else spec.lens[-1]
     tables, NB, _ = _tables(lens, spec.bs, 0, spec.spare, rng, spec.pool)
     maxb = -(-int(max_len) // spec.bs)

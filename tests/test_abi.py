@@ -1,0 +1,63 @@
+"""The C-ABI library loads on a machine without a GPU and exports every
+function include/pa.h declares; host-side argument checks need no GPU."""
+
+import ctypes
+
+import pytest
+
+from paged_kv_cache_307_gb300 import build as B
+
+
+@pytest.fixture(scope="module")
+def pa():
+    B.build()
+    from paged_kv_cache_307_gb300 import _lib
+    return _lib
+
+
+def test_every_declared_symbol_is_exported(pa):
+    names = pa.declared_functions()
+    assert {"pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(pa.lib, n), n
+
+
+def test_version_and_error_text(pa):
+    assert pa.lib.pa_version() >= 100
+    assert b"aligned" in pa.lib.pa_strerror(-4)
+    assert b"block" in pa.lib.pa_strerror(1)
+
+
+def test_workspace_and_partition_arithmetic(pa):
+    # 64 seqs x 32 heads, 128 blocks of 16 -> 2048 tokens -> 4 partitions of 512
+    assert pa.partition_size(64, 32, 32, 128, 128, 16, 0) == 512
+    rows = 64 * 32 * 4
+    ml = (rows * 8 + 255) // 256 * 256
+    assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, 0) == ml + rows * 128 * 4
+    assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, -1) == 0          # never split
+    assert pa.partition_size(1, 8, 8, 32, 3, 4, 0) == 12                   # fits one partition
+    assert pa.partition_size(1, 8, 8, 32, 3, 4, 6) == -2                   # not a block multiple
+
+
+def test_host_side_rejections_launch_nothing(pa):
+    L = pa.lib
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: every call below is rejected first
+    # head_dim 48 unsupported
+    assert L.pa_decode(fake, fake, fake, fake, fake, 4, fake, 2, 8, 8, 48, 16, 10, 1.0, 0, null, 0, 1, null) == -2
+    # heads not a multiple of kv heads
+    assert L.pa_decode(fake, fake, fake, fake, fake, 4, fake, 2, 6, 4, 64, 16, 10, 1.0, 0, null, 0, 1, null) == -2
+    # block size 12 unsupported
+    assert L.pa_copy_blocks(fake, fake, fake, 3, 10, 12, 2, 64, 1, null) == -2
+    # unknown dtype
+    assert L.pa_reshape_and_cache(fake, fake, fake, 3, fake, fake, 10, 16, 2, 64, 7, null) == -3
+    # null pool
+    assert L.pa_copy_blocks(null, fake, fake, 3, 10, 16, 2, 64, 1, null) == -1
+    # misaligned pointer
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert L.pa_reshape_and_cache(fake, odd, fake, 3, fake, fake, 10, 16, 2, 64, 1, null) == -4
+    # split needed but no workspace (4 partitions)
+    assert L.pa_decode(fake, fake, fake, fake, fake, 128, fake, 2, 8, 8, 128, 16, 10, 1.0, 512, null, 0, 1,
+                       null) == -5
+    # empty inputs are a no-op success
+    assert L.pa_copy_blocks(null, null, null, 0, 10, 16, 2, 64, 1, null) == 0
