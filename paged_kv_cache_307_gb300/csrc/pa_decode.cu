@@ -19,7 +19,10 @@
 //    stages, completing on an mbarrier with transaction bytes.  A block id
 //    outside the pool is flagged and replaced by block 0, so no copy leaves
 //    the pool.
-//  * Consumer warps take the item's blocks round-robin.  Inside a warp, LPT
+//  * Consumer warps take the item's blocks round-robin, and each warp owns its
+//    own ring of SPW stages which it consumes strictly in order (a ring shared
+//    by several round-robin consumers lets a warp wait on a stage two phases
+//    ahead, where a parity wait matches the stale phase).  Inside a warp, LPT
 //    lanes share one token (each lane owns two 16-byte chunks of head_dim), so
 //    one warp covers TPW tokens per pass with conflict-free 16-byte shared
 //    loads.  Each lane group keeps its own online-softmax state (m, l, o) for
@@ -49,6 +52,7 @@ __device__ unsigned g_status_decode;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kSmemAlign = 1024;
 
 struct DecodeParams {
   void* out;
@@ -62,7 +66,7 @@ struct DecodeParams {
   int part_tokens, max_parts;
   long long n_virtual;
   float qscale;       // scale * log2(e)
-  int stages;
+  int spw;            // shared-memory stages per consumer warp
   uint32_t tile_bytes;
 };
 
@@ -107,8 +111,11 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   constexpr int NCW = kConsumerWarps;
   static_assert(LPT >= 1 && LPT <= 32 && (32 % LPT) == 0, "lane split");
 
-  const int S = p.stages;
-  extern __shared__ __align__(128) unsigned char smem[];
+  const int S = p.spw * kConsumerWarps;   // stages in total
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // TMA destinations must be 128-byte aligned: align the base explicitly
+  // (the host reserves kSmemAlign bytes of slack).
+  unsigned char* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
   unsigned char* tilesK = smem;
   unsigned char* tilesV = smem + (size_t)S * p.tile_bytes;
   float* mbuf = reinterpret_cast<float*>(tilesV + (size_t)S * p.tile_bytes);
@@ -129,7 +136,12 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   }
   __syncthreads();
 
-  uint32_t it = 0;  // position in this CTA's block stream, identical in every role
+  // Block i of an item goes to consumer warp i % NCW.  Each warp owns SPW
+  // stages and consumes them strictly in order, so every stage has one
+  // producer and one consumer that both walk its phases in order and a
+  // parity wait can never match a stale phase.  u = the warp's running block
+  // count (same arithmetic in every role); stage = w*SPW + u % SPW.
+  const int SPW = p.spw;
 
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
@@ -138,16 +150,19 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
       prefetch_tensormap(&mapV);
     }
     const uint64_t pol = policy_evict_first();
-    uint32_t issued = 0;
+    uint32_t base[NCW], issued[NCW];
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) base[w] = issued[w] = 0;
     for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
       Item item;
       if (!decode_item(p, v, item)) continue;
       const int32_t* row = p.block_tables + (size_t)item.b * p.max_blocks;
-      for (int j0 = item.jb; j0 < item.je; j0 += 32) {
-        const int n = min(32, item.je - j0);
+      const int nblk = item.je - item.jb;
+      for (int j0 = 0; j0 < nblk; j0 += 32) {
+        const int n = min(32, nblk - j0);
         int blk = 0;
         if (lane < n) {
-          blk = __ldg(&row[j0 + lane]);
+          blk = __ldg(&row[item.jb + j0 + lane]);
           if ((unsigned)blk >= (unsigned)p.num_blocks) {
             atomicOr(&g_status_decode, PA_DEV_BAD_BLOCK);
             blk = 0;    // keep every copy inside the pool
@@ -155,9 +170,14 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
         for (int i = 0; i < n; ++i) {
           const int bi = __shfl_sync(0xffffffffu, blk, i);
+          const int w = (j0 + i) % NCW;
+          uint32_t u = 0;
+#pragma unroll
+          for (int k = 0; k < NCW; ++k)
+            if (k == w) u = base[k] + (uint32_t)((j0 + i) / NCW);
           if (lane == 0 && !*abort_flag) {
-            const int st = it % S;
-            const uint32_t ph = (it / S) & 1u;
+            const int st = w * SPW + (int)(u % SPW);
+            const uint32_t ph = (u / SPW) & 1u;
             if (!mbar_wait(&empty[st], ph ^ 1u)) {
               atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
               *abort_flag = 1;
@@ -165,17 +185,25 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               mbar_arrive_expect_tx(&full[st], 2u * p.tile_bytes);
               tma_load_4d(tilesK + (size_t)st * p.tile_bytes, &mapK, &full[st], 0, item.kvh, 0, bi, pol);
               tma_load_4d(tilesV + (size_t)st * p.tile_bytes, &mapV, &full[st], 0, item.kvh, 0, bi, pol);
-              issued = it + 1;
+#pragma unroll
+              for (int k = 0; k < NCW; ++k)
+                if (k == w) issued[k] = u + 1;
             }
           }
-          ++it;
         }
       }
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) base[w] += nblk > w ? (uint32_t)((nblk - w + NCW - 1) / NCW) : 0u;
     }
-    // Never leave the CTA with TMA writes into its shared memory in flight.
+    // Never leave the CTA with TMA writes into its shared memory in flight:
+    // wait (bounded) for the last SPW loads issued into each warp's stages.
     if (lane == 0) {
-      const uint32_t first = issued > (uint32_t)S ? issued - S : 0u;
-      for (uint32_t k = first; k < issued; ++k) mbar_wait(&full[k % S], (k / S) & 1u);
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) {
+        const uint32_t first = issued[w] > (uint32_t)SPW ? issued[w] - SPW : 0u;
+        for (uint32_t u = first; u < issued[w]; ++u)
+          mbar_wait(&full[w * SPW + (int)(u % SPW)], (u / SPW) & 1u);
+      }
     }
     return;
   }
@@ -185,6 +213,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   const int li = lane % LPT;      // chunk owner within the token row
   const int c0 = li, c1 = li + LPT;
   const int ctid = threadIdx.x;   // 0 .. NCW*32-1
+  uint32_t wcount = 0;            // blocks this warp has consumed so far
 
   for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
     Item item;
@@ -218,10 +247,9 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
 
     const int nblk = item.je - item.jb;
-    for (int i = 0; i < nblk; ++i, ++it) {
-      if (i % NCW != warp) continue;
-      const int st = it % S;
-      const uint32_t ph = (it / S) & 1u;
+    for (int i = warp; i < nblk; i += NCW, ++wcount) {
+      const int st = warp * SPW + (int)(wcount % SPW);
+      const uint32_t ph = (wcount / SPW) & 1u;
       bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
       if (live) {
         const bool late = !mbar_wait(&full[st], ph);
@@ -572,15 +600,16 @@ extern "C" int pa_decode(void* out, const void* query, const void* k_cache, cons
   prm.n_virtual = (long long)max_parts * prm.nsub * num_kv_heads * num_seqs;
   prm.qscale = scale * kLog2e;
   prm.tile_bytes = (uint32_t)(block_size * head_dim * elem_bytes(dtype));
-  // ~48 KB of K/V stages per CTA, at least 2.
-  int S = (int)(49152 / (2 * prm.tile_bytes));
-  S = S < 2 ? 2 : (S > 8 ? 8 : S);
-  prm.stages = S;
+  // ~64 KB of K/V stages per CTA: 1..4 stages per consumer warp.
+  int spw = (int)(65536 / (2 * prm.tile_bytes * kConsumerWarps));
+  spw = spw < 1 ? 1 : (spw > 4 ? 4 : spw);
+  prm.spw = spw;
+  const int S = spw * kConsumerWarps;
 
   const Launch L = dtype == PA_F32 ? pick1<float>(head_dim, GT) : pick1<__nv_bfloat16>(head_dim, GT);
   const size_t smem = 2 * (size_t)S * prm.tile_bytes +
                       (size_t)kConsumerWarps * GT * (head_dim + 2) * sizeof(float) +
-                      2 * (size_t)S * sizeof(uint64_t) + 16;
+                      2 * (size_t)S * sizeof(uint64_t) + 16 + kSmemAlign;
   const int occ = occupancy_for(L.kernel, smem, dev);
   if (occ <= 0) return PA_ERR_CUDA;
   long long grid = (long long)occ * device_sm_count();

@@ -37,7 +37,7 @@ def _cuda_case(name, **kw):
 
 # ------------------------------------------------------------------ append / copy
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c4b32", "c5"])
 def test_reshape_and_cache_bit_exact(pa, name):
     c = _cuda_case(name, small=True)
     exp_k, exp_v = oracle.reshape_and_cache(bits(c.key), bits(c.value), c.slot_mapping.cpu().numpy(),
