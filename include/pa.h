@@ -154,6 +154,11 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_p
  * Returns PA_ERR_CUDA if the device cannot be read. */
 int pa_last_error(void);
 
+/* Text of the last host-side failure on the calling thread (which CUDA call
+ * failed and why) after a call returned PA_ERR_CUDA; "" if none yet.  The
+ * string is owned by the library and overwritten by the next failure. */
+const char* pa_last_host_error(void);
+
 /* Human-readable text for a PA_ERR_* code or a PA_DEV_* bit. */
 const char* pa_strerror(int code);
 

@@ -41,13 +41,17 @@ lib.pa_last_error.argtypes = []
 lib.pa_last_error.restype = _i
 lib.pa_strerror.argtypes = [_i]
 lib.pa_strerror.restype = ctypes.c_char_p
+lib.pa_last_host_error.argtypes = []
+lib.pa_last_host_error.restype = ctypes.c_char_p
 lib.pa_version.argtypes = []
 lib.pa_version.restype = _i
 
 
 class PAError(RuntimeError):
     def __init__(self, code, what):
-        super().__init__("%s failed: %s (%d)" % (what, lib.pa_strerror(code).decode(), code))
+        extra = lib.pa_last_host_error().decode() if code == -6 else ""
+        super().__init__("%s failed: %s (%d)%s" % (what, lib.pa_strerror(code).decode(), code,
+                                                   (": " + extra) if extra else ""))
         self.code = code
 
 

@@ -4,8 +4,37 @@
 
 #include <cudaTypedefs.h>
 #include <mutex>
+#include <set>
+#include <stdio.h>
+#include <utility>
 
 namespace pa {
+
+static thread_local char g_host_msg[256] = "";
+
+void note_host_error(const char* what) { snprintf(g_host_msg, sizeof(g_host_msg), "%s", what); }
+
+bool ck(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return true;
+  snprintf(g_host_msg, sizeof(g_host_msg), "%s: %s", what, cudaGetErrorString(e));
+  return false;
+}
+
+bool raise_smem_limit(const void* kernel, int dev) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return true;
+  int optin = 0;
+  if (!ck(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+          "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)"))
+    return false;
+  if (!ck(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin),
+          "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)"))
+    return false;
+  done.insert({kernel, dev});
+  return true;
+}
 
 int device_sm_count() {
   static std::mutex mu;
@@ -82,3 +111,5 @@ extern "C" const char* pa_strerror(int code) {
 }
 
 extern "C" int pa_version(void) { return 100; }
+
+extern "C" const char* pa_last_host_error(void) { return pa::g_host_msg; }

@@ -103,7 +103,7 @@ extern "C" int pa_reshape_and_cache(const void* key, const void* value, const in
   reshape_and_cache_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
       (const unsigned char*)key, (const unsigned char*)value, slot_mapping, (unsigned char*)k_cache,
       (unsigned char*)v_cache, (long long)num_blocks * block_size, row_bytes);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return ck(cudaGetLastError(), "launch reshape_and_cache_kernel") ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
@@ -122,5 +122,5 @@ extern "C" int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs
   dim3 grid((unsigned)num_pairs, 2, spans);
   copy_blocks_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
       (unsigned char*)k_cache, (unsigned char*)v_cache, pairs, num_blocks, block_bytes, span);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return ck(cudaGetLastError(), "launch copy_blocks_kernel") ? PA_OK : PA_ERR_CUDA;
 }

@@ -159,6 +159,15 @@ int device_sm_count();
 bool encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int num_blocks,
                      int block_size, int num_kv_heads, int head_dim);
 
+// Host: record the text of the last host-side failure (per thread); read
+// back through pa_last_host_error().
+void note_host_error(const char* what);
+// Host: true if `e` is cudaSuccess, otherwise records "<what>: <error>".
+bool ck(cudaError_t e, const char* what);
+// Host: raise `kernel`'s dynamic shared-memory limit to the device opt-in
+// maximum (once per kernel and device).
+bool raise_smem_limit(const void* kernel, int dev);
+
 // Per-translation-unit status fetch (returns the sticky word and clears it).
 unsigned fetch_status_cache_ops();
 unsigned fetch_status_decode();

@@ -496,10 +496,13 @@ int occupancy_for(const void* kernel, size_t smem, int dev) {
   auto key = std::make_tuple(kernel, dev, smem);
   auto f = g_kinfo.find(key);
   if (f != g_kinfo.end()) return f->second.occupancy;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return 0;
+  // The dynamic shared-memory limit is a property of the kernel function, so
+  // raise it once to the device's opt-in maximum (never per launch size).
+  if (!raise_smem_limit(kernel, dev)) return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem) != cudaSuccess) return 0;
+  if (!ck(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem),
+          "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
+    return 0;
   g_kinfo[key] = KernelInfo{occ};
   return occ;
 }
@@ -569,11 +572,13 @@ extern "C" int pa_decode(void* out, const void* query, const void* k_cache, cons
   if (need && (!workspace || workspace_bytes < need)) return PA_ERR_WORKSPACE;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (!ck(cudaGetDevice(&dev), "cudaGetDevice")) return PA_ERR_CUDA;
   CUtensorMap mapK, mapV;
   if (!get_map(&mapK, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev) ||
-      !get_map(&mapV, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev))
+      !get_map(&mapV, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev)) {
+    note_host_error("cuTensorMapEncodeTiled failed for the K/V pool");
     return PA_ERR_CUDA;
+  }
 
   const int G = num_heads / num_kv_heads;
   const int GT = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
@@ -616,14 +621,15 @@ extern "C" int pa_decode(void* out, const void* query, const void* k_cache, cons
   if (grid > prm.n_virtual) grid = prm.n_virtual;
 
   void* args[] = {&mapK, &mapV, &prm};
-  if (cudaLaunchKernel(L.kernel, dim3((unsigned)grid), dim3(kThreads), args, smem, (cudaStream_t)stream) !=
-      cudaSuccess)
+  if (!ck(cudaLaunchKernel(L.kernel, dim3((unsigned)grid), dim3(kThreads), args, smem, (cudaStream_t)stream),
+          "cudaLaunchKernel(decode_kernel)"))
     return PA_ERR_CUDA;
   if (max_parts > 1) {
     const long long warps = (long long)num_seqs * num_heads;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     void* margs[] = {&prm};
-    if (cudaLaunchKernel(L.merge, dim3(blocks), dim3(256), margs, 0, (cudaStream_t)stream) != cudaSuccess)
+    if (!ck(cudaLaunchKernel(L.merge, dim3(blocks), dim3(256), margs, 0, (cudaStream_t)stream),
+            "cudaLaunchKernel(merge_kernel)"))
       return PA_ERR_CUDA;
   }
   return PA_OK;
