@@ -149,6 +149,31 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_p
                    int num_blocks, int block_size, int num_kv_heads, int head_dim,
                    pa_dtype dtype, void* stream);
 
+/*
+ * Causal chunked-prefill query tile over the paged cache ([OS] §8.1: a long
+ * prompt is processed in chunks, each continuing from the tokens already in
+ * the cache).  The tile is the LAST num_queries tokens of each sequence's
+ * context, their K/V already appended: query i of sequence b sits at
+ * position p = context_lens[b] - num_queries + i and attends to positions
+ * 0..p of its paged context (query head h reads KV head h / G).  Rows with
+ * p < 0 are written as zeros.
+ *
+ *   out, query  [num_seqs, num_queries, num_heads, head_dim]
+ *   other arguments as for pa_decode.
+ *
+ * Runs on the tcgen05 tensor cores: PA_BF16, head_dim 128, block_size in
+ * {8, 16, 32}, G = num_heads / num_kv_heads in {1, 2, 4, 8, 16}; anything
+ * else returns PA_ERR_SHAPE.  P is rounded to bf16 before the P*V product;
+ * accumulation is fp32.
+ */
+int pa_prefill_paged(void* out, const void* query, int num_queries,
+                     const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim,
+                     int block_size, int num_blocks, float scale,
+                     pa_dtype dtype, void* stream);
+
 /* Return the sticky device-detected condition bits (PA_DEV_*) and clear
  * them.  Synchronises the current device; 0 means nothing was detected.
  * Returns PA_ERR_CUDA if the device cannot be read. */

@@ -37,6 +37,8 @@ lib.pa_decode_partition_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 lib.pa_decode_partition_size.restype = _i
 lib.pa_copy_blocks.argtypes = [_p, _p, _i64p, _i, _i, _i, _i, _i, _i, _p]
 lib.pa_copy_blocks.restype = _i
+lib.pa_prefill_paged.argtypes = [_p, _p, _i, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
+lib.pa_prefill_paged.restype = _i
 lib.pa_last_error.argtypes = []
 lib.pa_last_error.restype = _i
 lib.pa_strerror.argtypes = [_i]
@@ -139,6 +141,19 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None):
     NB, bs, H, D = k_cache.shape
     _check(lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], NB, bs, H, D,
                               _dtype(k_cache), _stream(stream)), "pa_copy_blocks")
+
+
+def prefill(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=None):
+    """Causal chunked-prefill tile: q/out [B, Tq, Hq, D], the last Tq tokens
+    of each context."""
+    _contig(out, q, k_cache, v_cache, block_tables, context_lens)
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    B, Tq, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    _check(lib.pa_prefill_paged(_ptr(out), _ptr(q), Tq, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
+                                ctypes.c_float(scale), _dtype(q), _stream(stream)), "pa_prefill_paged")
+    return out
 
 
 def last_error():

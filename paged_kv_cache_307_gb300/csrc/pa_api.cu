@@ -83,14 +83,34 @@ bool encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int num_bl
   return r == CUDA_SUCCESS;
 }
 
+bool encode_map(CUtensorMap* map, const void* base, bool f32, int rank, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                  const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace pa
 
 extern "C" int pa_last_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   const unsigned a = pa::fetch_status_cache_ops();
   const unsigned b = pa::fetch_status_decode();
-  if (a == 0xffffffffu || b == 0xffffffffu) return PA_ERR_CUDA;
-  return (int)(a | b);
+  const unsigned c = pa::fetch_status_prefill();
+  if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) return PA_ERR_CUDA;
+  return (int)(a | b | c);
 }
 
 extern "C" const char* pa_strerror(int code) {

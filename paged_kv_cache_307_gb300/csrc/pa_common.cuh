@@ -159,6 +159,12 @@ int device_sm_count();
 bool encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int num_blocks,
                      int block_size, int num_kv_heads, int head_dim);
 
+// Host: encode a tiled tensor map of rank <= 5 (dims/box innermost first,
+// strides in bytes for dims 1..rank-1), bf16 or fp32, optionally with the
+// 128-byte shared-memory swizzle.  Returns false on failure.
+bool encode_map(CUtensorMap* map, const void* base, bool f32, int rank, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, bool swizzle128);
+
 // Host: record the text of the last host-side failure (per thread); read
 // back through pa_last_host_error().
 void note_host_error(const char* what);
@@ -171,5 +177,6 @@ bool raise_smem_limit(const void* kernel, int dev);
 // Per-translation-unit status fetch (returns the sticky word and clears it).
 unsigned fetch_status_cache_ops();
 unsigned fetch_status_decode();
+unsigned fetch_status_prefill();
 
 }  // namespace pa

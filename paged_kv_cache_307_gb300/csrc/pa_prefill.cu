@@ -1,0 +1,437 @@
+// pa_prefill.cu — causal chunked-prefill query tile over the paged KV cache,
+// on the 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM).
+//
+// What it computes ("LLM 推理引擎的内存管理与调度…" §8.1, chunked prefill; the
+// block-table addressing of its §三 and of "19.2 KV Cache 系统化管理"
+// §19.2.3): the last Tq tokens of each sequence's context are the query tile;
+// query i sits at position p = L - Tq + i and attends with softmax to the
+// keys at positions 0..p of its paged context.  Rows with p < 0 are zeros.
+//
+// How (GB300), one CTA per (query tile, sequence, KV head):
+//  * Rows = 128 (query position, head) pairs that share one KV head: QP =
+//    128/G positions x G query heads (GQA packing), so every K/V tile is
+//    loaded once for all G heads.  D = 128.
+//  * Warp 0 (TMA): the Q tile (two 64-column halves, 128-byte swizzle) once,
+//    then per 128-key tile the K and V rows of each physical block (box {64,
+//    1 head, bs, 1 block} per half) into a 2-stage ring.  Warp 1 (MMA):
+//    allocates 256 TMEM columns and issues, per key tile, S = Q K^T
+//    (M = N = 128, K = 128: 8 tcgen05.mma) into TMEM columns 0..127 and, once
+//    the softmax has written P, O += P V (V as an MN-major operand) into
+//    columns 128..255.  Warps 2-5 (softmax): one thread per row loads its S
+//    row from TMEM, applies the causal mask and scale (base 2), keeps a
+//    running max and sum, writes P = exp2(s - m) as bf16 into shared memory
+//    in the operand's swizzled layout, and at the end reads O back, divides
+//    by the sum and stores bf16 rows.
+//  * The running max used as the exponent reference only moves when a new
+//    maximum exceeds it by more than 2^8; then the row's O is rescaled in
+//    TMEM.  The sum and O always share the same reference, so the final
+//    quotient is exact up to rounding.
+//  * V rows at keys >= L (the unfilled tail of the last block, or blocks not
+//    loaded) are zeroed in shared memory before P V reads them: those slots
+//    may hold anything, and 0 * NaN would poison the product.
+//  * Every wait is bounded (2 s); a timeout sets PA_DEV_TIMEOUT, the roles
+//    wind down, outstanding TMA loads and MMAs are drained, TMEM is freed.
+#include "pa_tc.cuh"
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_status_prefill;
+
+constexpr int kThreads = 192;          // 6 warps
+constexpr int kTile = 128;             // rows and keys per tile
+constexpr int kD = 128;
+constexpr uint32_t kHalf = 16384;      // one 128-row x 64-column bf16 half tile
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = 32768;      // 2 stages x 32 KB
+constexpr uint32_t kOffV = 98304;      // 2 stages x 32 KB
+constexpr uint32_t kOffP = 163840;     // 32 KB
+constexpr uint32_t kOffBar = 196608;
+constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;   // + barriers + alignment slack
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+struct PrefillParams {
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int B, Tq, Hq, Hkv, G, QP, n_qt;
+  int max_blocks, bs, num_blocks;
+  float qscale;
+};
+
+struct Bars {
+  uint64_t q, full_k[2], full_v[2], empty[2], s, p, o, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity)) return true;
+  atomicOr(&g_status_prefill, PA_DEV_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+               const __grid_constant__ CUtensorMap mapV, const PrefillParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------------- work item
+  const int per = p.B * p.Hkv;
+  const int qt = p.n_qt - 1 - (int)(blockIdx.x / per);      // longest tiles first
+  const int rem = (int)(blockIdx.x % per);
+  const int b = rem / p.Hkv;
+  const int kvh = rem % p.Hkv;
+  const int q0 = qt * p.QP;
+  int L = __ldg(&p.context_lens[b]);
+  const int Lmax = p.max_blocks * p.bs;
+  if (L < 0 || L > Lmax) {
+    if (threadIdx.x == 0 && qt == p.n_qt - 1 && kvh == 0) atomicOr(&g_status_prefill, PA_DEV_BAD_LEN);
+    L = L < 0 ? 0 : Lmax;
+  }
+  const int pos0 = L - p.Tq + q0;                 // position of the tile's first query
+  const int kend = min(L, pos0 + p.QP);           // keys this tile needs: [0, kend)
+  const int nt = kend > 0 ? (kend + kTile - 1) / kTile : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->full_k[s], 1);
+      mbar_init(&bars->full_v[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->s, 1);
+    mbar_init(&bars->p, 128);
+    mbar_init(&bars->o, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t tS = tmem, tO = tmem + 128;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int issued_q = 0, issued = 0;
+    if (nt > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&mapQ);
+        prefetch_tensormap(&mapK);
+        prefetch_tensormap(&mapV);
+        mbar_arrive_expect_tx(&bars->q, 2 * kHalf);
+        const uint64_t pol = policy_evict_first();
+        tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, q0, b, pol);
+        tma_load_4d(smem + kOffQ + kHalf, &mapQ, &bars->q, 64, kvh * p.G, q0, b, pol);
+      }
+      issued_q = 1;
+      const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by other query tiles
+      const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
+      const int nbt = kTile / p.bs;
+      const uint32_t rows_bytes = (uint32_t)p.bs * 128u;    // one half-box
+      for (int j = 0; j < nt; ++j) {
+        const int st = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1);
+        const int k0 = j * kTile;
+        const int nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
+        int blk = 0;
+        if (lane < nvalid) {
+          blk = __ldg(&row[k0 / p.bs + lane]);
+          if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            atomicOr(&g_status_prefill, PA_DEV_BAD_BLOCK);
+            blk = 0;
+          }
+        }
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(&bars->empty[st], (u & 1u) ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->full_k[st], (uint32_t)nvalid * 2u * rows_bytes);
+          mbar_arrive_expect_tx(&bars->full_v[st], (uint32_t)nvalid * 2u * rows_bytes);
+        }
+        for (int jj = 0; jj < nvalid; ++jj) {
+          const int bi = __shfl_sync(0xffffffffu, blk, jj);
+          if (lane == 0) {
+            unsigned char* kdst = smem + kOffK + st * 2 * kHalf + jj * rows_bytes;
+            unsigned char* vdst = smem + kOffV + st * 2 * kHalf + jj * rows_bytes;
+            tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, bi, pol);
+            tma_load_4d(kdst + kHalf, &mapK, &bars->full_k[st], 64, kvh, 0, bi, pol);
+            tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, bi, pol);
+            tma_load_4d(vdst + kHalf, &mapV, &bars->full_v[st], 64, kvh, 0, bi, pol);
+          }
+        }
+        issued = j + 1;
+      }
+    }
+    // drain: no TMA write may land after the CTA exits
+    if (lane == 0) {
+      if (issued_q) mbar_wait(&bars->q, 0);
+      for (int j = max(0, issued - 2); j < issued; ++j) {
+        mbar_wait(&bars->full_k[j & 1], (uint32_t)(j >> 1) & 1u);
+        mbar_wait(&bars->full_v[j & 1], (uint32_t)(j >> 1) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      if (wait_or_abort(&bars->q, 0, abort_flag)) {
+        tc_fence_after();
+        for (int j = 0; j < nt; ++j) {
+          const int st = j & 1;
+          const uint32_t u = (uint32_t)(j >> 1);
+          if (!wait_or_abort(&bars->full_k[st], u & 1u, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kb = sbase + kOffK + st * 2 * kHalf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+            umma_bf16(tS, sdesc_sw128(sbase + kOffQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
+                      kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->s);
+          if (!wait_or_abort(&bars->p, (uint32_t)j & 1u, abort_flag)) break;
+          if (!wait_or_abort(&bars->full_v[st], u & 1u, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t vb = sbase + kOffV + st * 2 * kHalf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t poff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+            umma_bf16(tO, sdesc_sw128(sbase + kOffP + poff, 16, 1024),
+                      sdesc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024), idO, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars->o);
+          umma_commit(&bars->empty[st]);
+        }
+      }
+      // drain: every MMA issued so far has completed before TMEM is freed
+      umma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;            // tile row
+    const int qi = r / p.G, hh = r % p.G;
+    const int pos = pos0 + qi;
+    const bool row_out = (q0 + qi) < p.Tq;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float m_ref = -INFINITY, lsum = 0.f;
+    bool live = true;
+
+    for (int j = 0; j < nt && live; ++j) {
+      const int st = j & 1;
+      const uint32_t u = (uint32_t)(j >> 1);
+      const int k0 = j * kTile;
+      bool ok = wait_or_abort(&bars->s, (uint32_t)j & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
+      tc_fence_after();
+      float s[kTile];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + lane_off + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTile; ++c) {
+        const float x = (k0 + c <= pos) ? s[c] * p.qscale : -INFINITY;
+        s[c] = x;
+        mx = fmaxf(mx, x);
+      }
+      const bool need = mx > m_ref + kRescaleThreshold;   // false while mx is -inf
+      const float alpha = need ? exp2f(m_ref - mx) : 1.f; // m_ref = -inf gives 0
+      if (need) m_ref = mx;
+      if (j > 0) {
+        ok = wait_or_abort(&bars->o, (uint32_t)(j - 1) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + lane_off + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      lsum *= alpha;
+      // V rows at keys >= L hold no context: zero them once the tile has landed
+      if (k0 + r >= L) {
+        ok = wait_or_abort(&bars->full_v[st], u & 1u, abort_flag);
+        if (ok) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+          unsigned char* vrow = smem + kOffV + st * 2 * kHalf + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = z;
+            *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
+          }
+        }
+      }
+      // P = exp2(s - m_ref) as bf16, written in the 128-byte-swizzled K-major layout
+      unsigned char* prow = smem + kOffP + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = s[ch * 8 + 2 * e], x1 = s[ch * 8 + 2 * e + 1];
+          const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_ref);
+          const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_ref);
+          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+          lsum += __low2float(pk) + __high2float(pk);
+          w[e] = *reinterpret_cast<const uint32_t*>(&pk);
+        }
+        const int half = ch >> 3, chunk = ch & 7;
+        *reinterpret_cast<uint4*>(prow + half * kHalf + ((chunk ^ (r & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p);
+    }
+
+    // epilogue: O / l -> bf16 rows
+    bool have = nt > 0 && live;
+    if (have) {
+      const bool ok = wait_or_abort(&bars->o, (uint32_t)(nt - 1) & 1u, abort_flag);
+      have = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    unsigned char* orow = static_cast<unsigned char*>(p.out) +
+                          (((size_t)b * p.Tq + q0 + qi) * p.Hq + (size_t)kvh * p.G + hh) * (kD * 2);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tO + lane_off + c * 32, v);
+        tmem_ld_wait();
+      }
+      if (row_out) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a0 = have ? __uint_as_float(v[g * 8 + 2 * e]) * inv : 0.f;
+            const float a1 = have ? __uint_as_float(v[g * 8 + 2 * e + 1]) * inv : 0.f;
+            const __nv_bfloat162 pk = __floats2bfloat162_rn(a0, a1);
+            w[e] = *reinterpret_cast<const uint32_t*>(&pk);
+          }
+          st_v4(orow + (c * 32 + g * 8) * 2, make_uint4(w[0], w[1], w[2], w[3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+
+unsigned fetch_status_prefill() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_prefill, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (v && cudaMemcpyToSymbol(g_status_prefill, &zero, sizeof(zero)) != cudaSuccess) return 0xffffffffu;
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                                void* stream) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (dtype != PA_BF16 || head_dim != 128) return PA_ERR_SHAPE;
+  if (num_seqs < 0 || num_queries < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+      !(block_size == 8 || block_size == 16 || block_size == 32))
+    return PA_ERR_SHAPE;
+  const int G = num_heads / num_kv_heads;
+  if (G > 16 || (128 % G) != 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0 || num_queries == 0) return PA_OK;
+  if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+
+  const int QP = 128 / G;
+  CUtensorMap mapQ, mapK, mapV;
+  {
+    const uint64_t dims[4] = {128, (uint64_t)num_heads, (uint64_t)num_queries, (uint64_t)num_seqs};
+    const uint64_t str[3] = {256, (uint64_t)num_heads * 256, (uint64_t)num_queries * num_heads * 256};
+    const uint32_t box[4] = {64, (uint32_t)G, (uint32_t)QP, 1};
+    if (!encode_map(&mapQ, query, false, 4, dims, str, box, true)) {
+      note_host_error("cuTensorMapEncodeTiled failed for the query tile");
+      return PA_ERR_CUDA;
+    }
+  }
+  {
+    const uint64_t dims[4] = {128, (uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
+    const uint64_t str[3] = {256, (uint64_t)num_kv_heads * 256, (uint64_t)block_size * num_kv_heads * 256};
+    const uint32_t box[4] = {64, 1, (uint32_t)block_size, 1};
+    if (!encode_map(&mapK, k_cache, false, 4, dims, str, box, true) ||
+        !encode_map(&mapV, v_cache, false, 4, dims, str, box, true)) {
+      note_host_error("cuTensorMapEncodeTiled failed for the K/V pool");
+      return PA_ERR_CUDA;
+    }
+  }
+  int dev = 0;
+  if (!ck(cudaGetDevice(&dev), "cudaGetDevice")) return PA_ERR_CUDA;
+  if (!raise_smem_limit(reinterpret_cast<const void*>(&prefill_kernel), dev)) return PA_ERR_CUDA;
+
+  PrefillParams prm;
+  prm.out = out;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.B = num_seqs;
+  prm.Tq = num_queries;
+  prm.Hq = num_heads;
+  prm.Hkv = num_kv_heads;
+  prm.G = G;
+  prm.QP = QP;
+  prm.n_qt = (num_queries + QP - 1) / QP;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.bs = block_size;
+  prm.num_blocks = num_blocks;
+  prm.qscale = scale * kLog2e;
+  const long long grid = (long long)prm.n_qt * num_seqs * num_kv_heads;
+  void* args[] = {&mapQ, &mapK, &mapV, &prm};
+  if (!ck(cudaLaunchKernel(reinterpret_cast<const void*>(&prefill_kernel), dim3((unsigned)grid), dim3(kThreads),
+                           args, kSmemBytes, (cudaStream_t)stream),
+          "cudaLaunchKernel(prefill_kernel)"))
+    return PA_ERR_CUDA;
+  return PA_OK;
+}

@@ -297,27 +297,48 @@ def cow_case(small=False, device="cpu", seed=None, prompts=None):
             "prompt_len": plen, "prompt_blocks": prompt_blocks, "samples": S, "block_size": bs}
 
 
-def prefill_case(small=False, device="cpu", seed=None, prompts=None, Tq=512, prefix=1024):
-    """Chunked-prefill tile: per prompt, a ``prefix``-token paged context whose
-    last ``Tq`` tokens are the query tile (their K/V are already in the pool).
-    q: [P, Tq, Hq, D]."""
+def prefill_case(small=False, device="cpu", seed=None, prompts=None, Tq=512, prefix=1024,
+                 Hq=None, Hkv=None, bs=None, lens=None, nan_fill=True):
+    """Chunked-prefill tile: per prompt, a ``prefix``-token paged context
+    (or per-prompt ``lens``) whose last ``Tq`` tokens are the query tile
+    (their K/V are already in the pool).  q: [P, Tq, Hq, D].  Defaults are the
+    c5 shapes (GQA 32/8, D 128, bs 16)."""
     spec = SPECS["c5"]
     seed = (spec.seed if seed is None else seed) + 200
     rng = np.random.default_rng(seed)
-    P = prompts or (2 if small else 64)
-    bs = spec.bs
-    lens = np.full(P, prefix, dtype=np.int64)
+    Hq = Hq or spec.Hq
+    Hkv = Hkv or spec.Hkv
+    bs = bs or spec.bs
+    if lens is None:
+        P = prompts or (2 if small else 64)
+        lens = np.full(P, prefix, dtype=np.int64)
+    else:
+        lens = np.asarray(lens, dtype=np.int64)
+        P = len(lens)
     tables, NB, _ = _tables(lens, bs, 0, spec.spare, rng)
     dt = DTYPES[spec.dtype]
     gen = _generator(device, seed)
-    k = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
-    v = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
-    q = _randn((P, Tq, spec.Hq, spec.D), dt, gen, device)
+    k = _randn((NB, bs, Hkv, spec.D), dt, gen, device)
+    v = _randn((NB, bs, Hkv, spec.D), dt, gen, device)
+    q = _randn((P, Tq, Hq, spec.D), dt, gen, device)
     tables_t = torch.from_numpy(tables)
-    _nan_unused(k, v, tables_t, lens, bs, True)
+    _nan_unused(k, v, tables_t, lens, bs, nan_fill)
     return {"q": q, "k_cache": k, "v_cache": v, "block_tables": tables_t.to(device),
             "context_lens": torch.from_numpy(lens.astype(np.int32)).to(device),
-            "scale": scale_for(spec.D), "Tq": Tq}
+            "scale": scale_for(spec.D), "Tq": Tq, "block_size": bs}
+
+
+def prefill_flops(lens, Tq, Hq, D):
+    """Multiply-add FLOPs of the causal tile (QK^T and PV, 2 flops per MAC),
+    counting only unmasked (query, key) pairs."""
+    tot = 0
+    for L in lens:
+        L = int(L)
+        for i in range(Tq):
+            pos = L - Tq + i
+            if pos >= 0:
+                tot += pos + 1
+    return 4 * tot * Hq * D
 
 
 def algorithmic_decode_bytes(case):

@@ -185,6 +185,7 @@ def test_shared_prefix_equals_private_copies(pa):
     k = torch.cat([c.k_cache, torch.empty((need,) + c.k_cache.shape[1:], dtype=c.k_cache.dtype,
                                           device="cuda")])
     v = torch.cat([c.v_cache, torch.empty_like(k[c.num_blocks:])])
+    tables[tables == c.num_blocks] = k.shape[0]        # unused entries stay out of range
     nxt = c.num_blocks
     pairs = []
     for b in range(c.q.shape[0]):
@@ -194,7 +195,6 @@ def test_shared_prefix_equals_private_copies(pa):
             pairs.append((int(tables[b, j]), nxt))
             tables[b, j] = nxt
             nxt += 1
-    tables[tables == c.num_blocks] = k.shape[0]
     pa.copy_blocks(k, v, torch.tensor(pairs, dtype=torch.int64, device="cuda"))
     c.k_cache, c.v_cache = k, v
     c.block_tables = torch.from_numpy(tables).cuda()

@@ -1,0 +1,101 @@
+"""Chunked-prefill tile on the tensor cores (through the C ABI) against the
+float64 oracle.  bf16 inputs, fp32 accumulation, P rounded to bf16: the
+bf16 tolerance applies (max 2e-2, mean 2e-3)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_307_gb300 import workloads as W
+from _helpers import f64, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from paged_kv_cache_307_gb300 import build
+    build.build()
+    from paged_kv_cache_307_gb300 import _lib
+    assert torch.cuda.is_available()
+    _lib.last_error()
+    return _lib
+
+
+def _oracle(case, seqs=None):
+    lens = case["context_lens"].cpu().numpy()
+    tables = case["block_tables"].cpu().numpy()
+    bs = case["block_size"]
+    seqs = list(range(len(lens))) if seqs is None else list(seqs)
+    used = sorted({int(tables[b, j]) for b in seqs for j in range(-(-int(lens[b]) // bs))})
+    index = {blk: i for i, blk in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=case["k_cache"].device)
+    k = f64(case["k_cache"].index_select(0, idx))
+    v = f64(case["v_cache"].index_select(0, idx))
+    nt = np.zeros((len(seqs), tables.shape[1]), dtype=np.int64)
+    for r, b in enumerate(seqs):
+        for j in range(-(-int(lens[b]) // bs)):
+            nt[r, j] = index[int(tables[b, j])]
+    q = f64(case["q"])[seqs]
+    return oracle.paged_prefill(q, k, v, nt, lens[seqs], case["scale"])
+
+
+def _run(pa, case):
+    out = torch.full_like(case["q"], float("nan"))
+    pa.prefill(out, case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+               case["context_lens"], case["scale"])
+    torch.cuda.synchronize()
+    return out
+
+
+def test_prefill_c5_small(pa):
+    case = W.prefill_case(small=True, device="cuda")
+    ref = _oracle(case)
+    out = _run(pa, case)
+    assert pa.last_error() == 0
+    assert_close(f64(out), ref, "bf16")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (32, 4), (32, 2)])
+def test_prefill_group_sizes(pa, Hq, Hkv):
+    case = W.prefill_case(device="cuda", Hq=Hq, Hkv=Hkv, Tq=160, lens=[300, 161])
+    ref = _oracle(case)
+    out = _run(pa, case)
+    assert pa.last_error() == 0
+    assert_close(f64(out), ref, "bf16")
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_prefill_block_sizes_and_ragged_tails(pa, bs):
+    # lengths that end mid-block and mid-tile, one shorter than the tile
+    case = W.prefill_case(device="cuda", bs=bs, Tq=200, lens=[131, 517, 77])
+    ref = _oracle(case)
+    out = _run(pa, case)
+    assert pa.last_error() == 0
+    got = f64(out)
+    assert not got[2, :200 - 77].any()          # rows before position 0 are zero
+    assert_close(got, ref, "bf16")
+
+
+def test_prefill_single_query_equals_decode(pa):
+    """Tq = 1 is a decode step: the tile row equals pa_decode's output."""
+    case = W.prefill_case(device="cuda", Tq=1, lens=[700, 33, 1024])
+    out = _run(pa, case)
+    dec = torch.empty_like(case["q"][:, 0])
+    pa.decode(dec, case["q"][:, 0].contiguous(), case["k_cache"], case["v_cache"], case["block_tables"],
+              case["context_lens"], case["scale"])
+    torch.cuda.synchronize()
+    assert_close(f64(out[:, 0]), f64(dec), "bf16")
+    assert_close(f64(out), _oracle(case), "bf16")
+
+
+def test_prefill_full_size_sampled(pa):
+    case = W.prefill_case(device="cuda")
+    seqs = [0, 37]
+    ref = _oracle(case, seqs)
+    out = _run(pa, case)
+    assert pa.last_error() == 0
+    got = f64(out)
+    assert np.isfinite(got).all()
+    assert_close(got[seqs], ref, "bf16")
