@@ -123,6 +123,38 @@ int pa_decode(void* out, const void* query,
               void* workspace, size_t workspace_bytes,
               pa_dtype dtype, void* stream);
 
+/*
+ * Decode that allocates nothing and takes no workspace.  This entry point
+ * has no counterpart on the paged-attention pages; it exists for callers
+ * that cannot allocate device memory at the point of the call — for example
+ * a plug-in whose host engine owns every device allocation through its own
+ * pool, or a latency-critical path that cannot afford an allocation call
+ * that may synchronise the device.
+ *
+ * Same arguments and result as pa_decode, without workspace: the split-K
+ * scratch is a PA_NOALLOC_SCRATCH_BYTES array compiled into the library,
+ * held by every device that loads the library until the process exits.
+ *  - Sizes whose pa_decode_workspace_bytes() exceeds that limit are rejected
+ *    with PA_ERR_WORKSPACE (nothing launched; pa_last_host_error() says how
+ *    much was needed).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and it keeps the previous
+ *    call's contents: calls whose GPU work overlaps (e.g. on two streams)
+ *    race on it and must be ordered by the caller.  Nothing in it needs to
+ *    start at zero.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int pa_decode_noalloc(void* out, const void* query,
+                      const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs,
+                      int num_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, float scale, int partition_size,
+                      pa_dtype dtype, void* stream);
+
 /* Bytes of workspace pa_decode needs for these sizes (0 when no sequence can
  * span more than one partition).  Pure host arithmetic; no CUDA call. */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,

@@ -31,6 +31,8 @@ lib.pa_reshape_and_cache.argtypes = [_p, _p, _i64p, _i, _p, _p, _i, _i, _i, _i, 
 lib.pa_reshape_and_cache.restype = _i
 lib.pa_decode.argtypes = [_p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _i, _p]
 lib.pa_decode.restype = _i
+lib.pa_decode_noalloc.argtypes = [_p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
+lib.pa_decode_noalloc.restype = _i
 lib.pa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 lib.pa_decode_workspace_bytes.restype = _sz
 lib.pa_decode_partition_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]

@@ -43,6 +43,7 @@
 #include <mutex>
 #include <map>
 #include <tuple>
+#include <stdio.h>
 
 namespace pa {
 namespace {
@@ -633,4 +634,67 @@ extern "C" int pa_decode(void* out, const void* query, const void* k_cache, cons
       return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// Some callers cannot allocate device memory when they call in: a plug-in
+// hosted by an engine that owns every device allocation through its own pool
+// (and budgets it up front), or a latency-critical path that cannot afford an
+// allocation call that may synchronise the device.  pa_decode_noalloc serves
+// them by using a scratch array compiled into this library as the split-K
+// workspace.  Every device that loads the library holds the array until the
+// process exits.  The array is shared by every call on a device: calls whose
+// GPU work overlaps in time (for instance on two streams) race on it, so they
+// must be ordered.  Nothing in it needs to start at zero: every value a call
+// reads was written earlier by the same call.
+namespace pa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)PA_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address has to come
+// from cudaGetSymbolAddress, once per device, with that device current.
+void* scratch_address(int dev) {
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (!ck(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress(no-alloc scratch)"))
+      return nullptr;
+    g_scratch_ptr[dev] = ptr;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_noalloc(void* out, const void* query, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int num_blocks, float scale,
+                                 int partition_size, pa_dtype dtype, void* stream) {
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                block_size, partition_size);
+  if (need > pa::kNoAllocScratchBytes) {
+    char msg[160];
+    snprintf(msg, sizeof(msg), "pa_decode_noalloc: these sizes need %zu bytes of scratch; the built-in array "
+             "holds %zu", need, pa::kNoAllocScratchBytes);
+    pa::note_host_error(msg);
+    return PA_ERR_WORKSPACE;
+  }
+  int dev = 0;
+  if (!pa::ck(cudaGetDevice(&dev), "cudaGetDevice")) return PA_ERR_CUDA;
+  void* scratch = pa::scratch_address(dev);
+  if (!scratch) return PA_ERR_CUDA;
+  return pa_decode(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                   num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size, scratch,
+                   pa::kNoAllocScratchBytes, dtype, stream);
 }
