@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -262,7 +263,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     spec = W.SPECS[args.workload]
-    case = W.decode_case(args.workload, device=dev, nan_fill=False, seed=spec.seed + 1000 * rank)
+    case = W.decode_case(args.workload, device=dev, nan_fill=False, seed=spec.seed + 1000 * rank,
+                         B=args.batch or None)
     Bsz, Hq, D = case.q.shape
     ws = pa.alloc_workspace(case.q, case.k_cache, case.block_tables, args.partition)
     out = torch.empty_like(case.q)
@@ -377,7 +379,7 @@ def run_ours(args, rank, world, local_rank):
         "pct_of_peak": round(100.0 * value / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode (decode_kernel + merge_kernel), %.4f ms per launch" % dec_ms,
+                     "kernel": "pa_decode (decode_kernel + merge_kernel), %.4f ms per call" % dec_ms,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -102,8 +102,10 @@ int pa_reshape_and_cache(const void* key, const void* value,
  *   block_tables   [num_seqs, max_blocks_per_seq] int32
  *   context_lens   [num_seqs] int32
  *   scale          the pages use 1/sqrt(head_dim)
- *   partition_size split-K partition in tokens: 0 = automatic, < 0 = never
- *                  split, > 0 = a multiple of block_size.  A sequence longer
+ *   partition_size split-K partition in tokens: 0 = automatic (512 tokens
+ *                  when num_heads == num_kv_heads, 2048 for grouped-query
+ *                  attention), < 0 = never split, > 0 = a multiple of
+ *                  block_size.  A sequence longer
  *                  than one partition is processed as independent partitions
  *                  whose (max, sum, unnormalised output) states are merged by
  *                  log-sum-exp in a second kernel.
@@ -112,7 +114,11 @@ int pa_reshape_and_cache(const void* key, const void* value,
  *                  contents on entry do not matter; calls that share one
  *                  workspace must be ordered (same stream).
  *
- * Output is fp32-accumulated; bf16 output is rounded to nearest even.
+ * Output is fp32-accumulated; bf16 output is rounded to nearest even.  With
+ * bf16, head_dim 64 or 128, block_size >= 8 and a power-of-two group G >= 2,
+ * the G query heads of a KV head are computed together on tensor cores
+ * (m16n8k16 bf16 products, fp32 accumulation; P is rounded to bf16 for the
+ * P*V product); otherwise on CUDA cores in fp32.
  */
 int pa_decode(void* out, const void* query,
               const void* k_cache, const void* v_cache,

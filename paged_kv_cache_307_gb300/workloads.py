@@ -30,7 +30,7 @@ set, so any read of them shows up in the output.  Unused block-table entries
 hold ``num_blocks`` (out of range).
 """
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 import math
 
 import numpy as np
@@ -163,13 +163,18 @@ def _tables(lens, bs, NB_min, spare, rng, fixed_pool=0):
     return tables, NB, perm[off:]
 
 
-def decode_case(name, small=False, device="cpu", nan_fill=True, seed=None, B=None, lens=None):
+def decode_case(name, small=False, device="cpu", nan_fill=True, seed=None, B=None, lens=None,
+                len_dist=None, **over):
     """Build one decode workload.  The pool holds every token of every context
     except each sequence's newest one (position L-1), whose K/V arrive in
     ``key``/``value`` with its slot in ``slot_mapping``: the caller appends,
     then attends (context_lens count the newest token).  ``lens`` overrides
-    the drawn context lengths (and the batch size)."""
-    spec = SPECS[name]
+    the drawn context lengths (and the batch size), ``len_dist`` the length
+    distribution; other keywords replace fields of the workload's Spec
+    (e.g. Hq, Hkv, D, bs)."""
+    if len_dist is not None:
+        over["lens"] = len_dist
+    spec = replace(SPECS[name], **over) if over else SPECS[name]
     seed = spec.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     if lens is not None:

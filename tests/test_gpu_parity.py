@@ -116,7 +116,7 @@ def test_decode_ragged_boundaries(pa, lens, partition):
     assert_close(f64(out), ref, "bf16")
 
 
-@pytest.mark.parametrize("G", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 16, 32])
 def test_decode_gqa_group_sizes(pa, G):
     c = _cuda_case("c4", small=True)
     # reuse the c4 pool (8 KV heads) with G query heads per KV head
@@ -125,6 +125,19 @@ def test_decode_gqa_group_sizes(pa, G):
     c.spec = W.Spec(**{**c.spec.__dict__, "Hq": 8 * G})
     ref = oracle_decode(c)
     out = gpu_decode(c)
+    assert pa.last_error() == 0
+    assert_close(f64(out), ref, "bf16")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(16, 4, 64, 8), (32, 8, 64, 32), (8, 2, 128, 8), (16, 8, 128, 32),
+                                         (12, 4, 128, 16), (8, 4, 32, 16), (8, 2, 128, 4)])
+@pytest.mark.parametrize("partition", [0, -1])
+def test_decode_shape_variants(pa, Hq, Hkv, D, bs, partition):
+    """Tensor-core GQA path (bf16, head_dim 64/128, G a power of two, block
+    size >= 8) and the CUDA-core path for the rest, against the oracle."""
+    c = _cuda_case("c4", B=3, Hq=Hq, Hkv=Hkv, D=D, bs=bs, len_dist=("uniform", 1, 1500))
+    ref = oracle_decode(c)
+    out = gpu_decode(c, partition_size=partition)
     assert pa.last_error() == 0
     assert_close(f64(out), ref, "bf16")
 
