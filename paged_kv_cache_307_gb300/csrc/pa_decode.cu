@@ -229,9 +229,10 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                     tma_load_4d(tilesK + o2, &mapK, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
                     tma_load_4d(tilesV + o2, &mapV, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
                   }
-                } else {
-                  tma_load_4d(tilesK + off, &mapK, &full[st], 0, item.kvh0 + hl, 0, bi, pol);
-                  tma_load_4d(tilesV + off, &mapV, &full[st], 0, item.kvh0 + hl, 0, bi, pol);
+                } else if (hl == 0) {
+                  // one box {D, HG heads, bs, 1}: smem [bs][HG][D], 1 KB rows for HG = 4
+                  tma_load_4d(tilesK + off, &mapK, &full[st], 0, item.kvh0, 0, bi, pol);
+                  tma_load_4d(tilesV + off, &mapV, &full[st], 0, item.kvh0, 0, bi, pol);
                 }
               }
 #pragma unroll
@@ -464,8 +465,9 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         }
         if (live) {
           const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
-          const unsigned char* kt = tilesK + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
-          const unsigned char* vt = tilesV + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
+          // stage layout [bs][HG][D]: token t of head hl at (t*HG + hl) * ROW
+          const unsigned char* kt = tilesK + (size_t)st * stage_bytes + (size_t)hl * ROW;
+          const unsigned char* vt = tilesV + (size_t)st * stage_bytes + (size_t)hl * ROW;
           for (int tb = 0; tb < valid; tb += TPW * NS) {
             float s[NS][GT];
   #pragma unroll
@@ -477,8 +479,8 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               for (int h = 0; h < GT; ++h) part[h] = 0.f;
               if (ok) {
                 float kf[DPL];
-                E::unpack(*reinterpret_cast<const uint4*>(kt + t * ROW + c0 * 16), kf);
-                E::unpack(*reinterpret_cast<const uint4*>(kt + t * ROW + c1 * 16), kf + EPC);
+                E::unpack(*reinterpret_cast<const uint4*>(kt + t * (HG * ROW) + c0 * 16), kf);
+                E::unpack(*reinterpret_cast<const uint4*>(kt + t * (HG * ROW) + c1 * 16), kf + EPC);
   #pragma unroll
                 for (int h = 0; h < GT; ++h)
   #pragma unroll
@@ -508,8 +510,8 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               const int t = tb + k * TPW + grp;
               if (t < valid) {
                 float vf[DPL];
-                E::unpack(*reinterpret_cast<const uint4*>(vt + t * ROW + c0 * 16), vf);
-                E::unpack(*reinterpret_cast<const uint4*>(vt + t * ROW + c1 * 16), vf + EPC);
+                E::unpack(*reinterpret_cast<const uint4*>(vt + t * (HG * ROW) + c0 * 16), vf);
+                E::unpack(*reinterpret_cast<const uint4*>(vt + t * (HG * ROW) + c1 * 16), vf + EPC);
   #pragma unroll
                 for (int h = 0; h < GT; ++h) {
                   const float pk = exp2f(s[k][h] - m[h]);
@@ -690,18 +692,19 @@ std::map<std::tuple<const void*, int, size_t>, KernelInfo> g_kinfo;  // (kernel,
 
 struct MapKey {
   const void* base;
-  int dt, nb, bs, h, d, dev, swz;
+  int dt, nb, bs, h, d, dev, swz, boxh;
   bool operator<(const MapKey& o) const {
-    return std::tie(base, dt, nb, bs, h, d, dev, swz) <
-           std::tie(o.base, o.dt, o.nb, o.bs, o.h, o.d, o.dev, o.swz);
+    return std::tie(base, dt, nb, bs, h, d, dev, swz, boxh) <
+           std::tie(o.base, o.dt, o.nb, o.bs, o.h, o.d, o.dev, o.swz, o.boxh);
   }
 };
 std::map<MapKey, CUtensorMap> g_maps;
 
-// swz = false: box {D, 1 head, bs, 1 block}, no swizzle (FFMA path).
+// swz = false: box {D, boxh heads, bs, 1 block}, no swizzle (CUDA-core path).
 // swz = true: box {64, 1 head, bs, 1 block}, 128-byte swizzle (tensor-core path).
-bool get_map(CUtensorMap* out, const void* base, pa_dtype dt, int nb, int bs, int h, int d, int dev, bool swz) {
-  MapKey key{base, (int)dt, nb, bs, h, d, dev, swz ? 1 : 0};
+bool get_map(CUtensorMap* out, const void* base, pa_dtype dt, int nb, int bs, int h, int d, int dev, bool swz,
+             int boxh) {
+  MapKey key{base, (int)dt, nb, bs, h, d, dev, swz ? 1 : 0, swz ? 1 : boxh};
   std::lock_guard<std::mutex> lk(g_mu);
   auto f = g_maps.find(key);
   if (f != g_maps.end()) {
@@ -716,7 +719,11 @@ bool get_map(CUtensorMap* out, const void* base, pa_dtype dt, int nb, int bs, in
     const uint32_t box[4] = {64, 1, (uint32_t)bs, 1};
     ok = encode_map(out, base, dt == PA_F32, 4, dims, str, box, true);
   } else {
-    ok = encode_pool_map(out, base, dt, nb, bs, h, d);
+    const uint64_t e = (uint64_t)elem_bytes(dt);
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)h, (uint64_t)bs, (uint64_t)nb};
+    const uint64_t str[3] = {d * e, (uint64_t)h * d * e, (uint64_t)bs * h * d * e};
+    const uint32_t box[4] = {(uint32_t)d, (uint32_t)boxh, (uint32_t)bs, 1};
+    ok = encode_map(out, base, dt == PA_F32, 4, dims, str, box, false);
   }
   if (!ok) return false;
   if (g_maps.size() > 64) g_maps.clear();
@@ -814,8 +821,12 @@ extern "C" int pa_decode(void* out, const void* query, const void* k_cache, cons
   // Tensor cores over the query group when it is a real contraction (G >= 2).
   const bool use_mma = dtype == PA_BF16 && (head_dim == 64 || head_dim == 128) && G >= 2 && (G & (G - 1)) == 0 &&
                        block_size >= 8;
-  if (!get_map(&mapK, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev, use_mma) ||
-      !get_map(&mapV, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev, use_mma)) {
+  // KV heads per work item: 4 on the tensor-core path (one warp per head,
+  // the four heads' tiles loaded back to back); 1 on the CUDA-core path,
+  // where a warp ring per head measured faster for MHA.
+  const int HG = use_mma ? (num_kv_heads % 4 == 0 ? 4 : num_kv_heads % 2 == 0 ? 2 : 1) : 1;
+  if (!get_map(&mapK, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev, use_mma, HG) ||
+      !get_map(&mapV, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, dev, use_mma, HG)) {
     note_host_error("cuTensorMapEncodeTiled failed for the K/V pool");
     return PA_ERR_CUDA;
   }
@@ -841,10 +852,7 @@ extern "C" int pa_decode(void* out, const void* query, const void* k_cache, cons
   prm.num_blocks = num_blocks;
   prm.part_tokens = P;
   prm.max_parts = max_parts;
-  // KV heads per item: 4 when they divide (one consumer warp per head, the
-  // four heads of a block requested together), else 2 or 1 with several
-  // warps per head.
-  prm.HG = use_mma ? (num_kv_heads % 4 == 0 ? 4 : num_kv_heads % 2 == 0 ? 2 : 1) : 1;
+  prm.HG = HG;
   prm.n_hg = num_kv_heads / prm.HG;
   prm.WPH = kConsumerWarps / prm.HG;
   prm.n_virtual = (long long)max_parts * prm.nsub * prm.n_hg * num_seqs;
