@@ -40,6 +40,8 @@ WORKLOAD_TEXT = {
     "c4": "bf16 GQA decode: 32/8 heads, head_dim 128, block_size 16, batch 256, context U[1024,32768], "
           "split-K 512; plus reshape_and_cache of 256 new tokens",
     "c4b32": "as c4 with block_size 32",
+    "c5prefill": "bf16 GQA 32/8 causal chunked-prefill tile: 64 prompts, 512 queries at positions 512..1023 "
+                 "over a 1024-token paged context (block_size 16), tensor cores",
     "c5": "bf16 GQA decode 32/8, 64 prompts x 8 samples sharing 1024-token prompts + private tails U[0,256]; "
           "plus reshape_and_cache of the new tokens",
 }
@@ -216,12 +218,45 @@ def cpu_baseline(name, seconds):
             "seq_steps_per_s": round(reps * nseq / dt, 3)}
 
 
+def run_reference_prefill(args):
+    """Oracle prefill on one host core: each step is a slice of the c5 tile
+    (one prompt, 8 query rows at the end of its 1024-token context)."""
+    import numpy as np
+    import torch
+    import oracle
+    from paged_kv_cache_307_gb300 import workloads as W
+    c = W.prefill_case(device="cpu", prompts=1, Tq=8, nan_fill=False)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    k, v, q = f64(c["k_cache"]), f64(c["v_cache"]), f64(c["q"])
+    tables, lens = c["block_tables"].numpy(), c["context_lens"].numpy()
+    flops = W.prefill_flops(lens, 8, q.shape[2], q.shape[3])
+    for _ in range(args.warmup):
+        oracle.paged_prefill(q, k, v, tables, lens, c["scale"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_prefill(q, k, v, tables, lens, c["scale"])
+    dt = time.perf_counter() - t0
+    val = flops * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": "chunked-prefill tile TFLOP/s (bf16, causal, unmasked work)",
+            "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "c5prefill: " + WORKLOAD_TEXT["c5prefill"],
+                       "sample": "one prompt, 8 query rows per step"},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d steps of 8 query rows x 32 heads over a 1024-token context" % args.steps},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle timed on one host core: each step is one (sequence, KV head)
     slice of the workload (append + decode), cycling through a 16-sequence
     sample, so K steps stay within minutes."""
     if rank != 0:
         return
+    if args.workload == "c5prefill":
+        return run_reference_prefill(args)
     tasks, nbytes = _cpu_tasks(args.workload, 16, seed=12345)
     for i in range(args.warmup):
         _oracle_slice(tasks[i % len(tasks)])
@@ -249,6 +284,114 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- GPU leg
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops_sustained"]), "measured sustained"
+    except Exception:
+        return 1700.0, "fallback sustained"
+
+
+def run_prefill(args, rank, world, local_rank):
+    """The c5 chunked-prefill tile: pa_prefill_paged over 64 prompts x 512
+    queries.  Metric: TFLOP/s of the unmasked causal work (QK^T and PV, two
+    flops per multiply-add)."""
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_307_gb300 import build as B
+    B.build()
+    from paged_kv_cache_307_gb300 import _lib as pa
+    from paged_kv_cache_307_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    case = W.prefill_case(device=dev, seed=W.SPECS["c5"].seed + 1000 * rank, nan_fill=False,
+                          prompts=args.batch or None)
+    q = case["q"]
+    P, Tq, Hq, D = q.shape
+    out = torch.empty_like(q)
+    lens = case["context_lens"].cpu().numpy()
+    flops = W.prefill_flops(lens, Tq, Hq, D)
+    stream = torch.cuda.current_stream()
+
+    def step(qq=q, tables=case["block_tables"], cl=case["context_lens"]):
+        pa.prefill(out, qq, case["k_cache"], case["v_cache"], tables, cl, case["scale"])
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pa.last_error() == 0
+    K = args.steps
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    sampler = ClockSampler(int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].isdigit()
+                           else local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    start.record(stream)
+    for _ in range(K):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert pa.last_error() == 0
+    step_s = total_ms / 1e3 / K
+    tflops = world * flops / step_s / 1e12
+
+    qh = q.cpu().pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd = torch.empty_like(q)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        step(qq=qd)
+        oh.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = min(K, 50)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = a.elapsed_time(b) / 1e3 / Ke
+    if rank != 0:
+        return
+    peak, src = tensor_peak()
+    line = {
+        "metric": "chunked-prefill tile TFLOP/s (bf16, causal, unmasked work)", "value": round(tflops, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "c5prefill: " + WORKLOAD_TEXT["c5prefill"], "prompts": P, "queries": Tq,
+                   "num_heads": Hq, "num_kv_heads": case["k_cache"].shape[2], "head_dim": D,
+                   "flops_per_step": flops,
+                   "l2": "K/V %.2f GB + Q/O %.2f GB per call (larger than L2); no flush"
+                         % (2 * case["k_cache"].numel() * 2 / 1e9, 2 * q.numel() * 2 / 1e9)},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4), "traffic": None,
+                     "kernel": "prefill_kernel (tcgen05.mma, TMEM accumulators)",
+                     "peak_source": "%s bf16 (MEASURED_PEAKS.json)" % src},
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": qh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
 
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -409,7 +552,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.workload == "c5prefill":
+            run_prefill(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -201,8 +201,8 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_p
  *
  * Runs on the tcgen05 tensor cores: PA_BF16, head_dim 128, block_size in
  * {8, 16, 32}, G = num_heads / num_kv_heads in {1, 2, 4, 8, 16}; anything
- * else returns PA_ERR_SHAPE.  P is rounded to bf16 before the P*V product;
- * accumulation is fp32.
+ * else returns PA_ERR_SHAPE, as does scale <= 0.  P is rounded to bf16 before
+ * the P*V product; accumulation is fp32.
  */
 int pa_prefill_paged(void* out, const void* query, int num_queries,
                      const void* k_cache, const void* v_cache,

@@ -210,35 +210,41 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < WPH; ++k)
             if (k == w) u = base[k] + (uint32_t)((j0 + i) / WPH);
+          const int st = w * SPW + (int)(u % SPW);
+          const uint32_t ph = (u / SPW) & 1u;
+          constexpr int HALVES = MMA ? D / 64 : 1;
+          constexpr int NOPS = MMA ? 2 * HG * HALVES : 2;   // TMA loads per block
+          int go = 0;
           if (lane == 0 && !*abort_flag) {
-            const int st = w * SPW + (int)(u % SPW);
-            const uint32_t ph = (u / SPW) & 1u;
             if (!mbar_wait(&empty[st], ph ^ 1u)) {
               atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
               *abort_flag = 1;
             } else {
               mbar_arrive_expect_tx(&full[st], 2u * stage_bytes);
-#pragma unroll
-              for (int hl = 0; hl < HG; ++hl) {
-                const size_t off = (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
-                if constexpr (MMA) {
-                  // 128-byte-swizzled halves of 64 columns: [half][bs rows][128 B]
-#pragma unroll
-                  for (int hh = 0; hh < D / 64; ++hh) {
-                    const size_t o2 = off + (size_t)hh * p.bs * 128;
-                    tma_load_4d(tilesK + o2, &mapK, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
-                    tma_load_4d(tilesV + o2, &mapV, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
-                  }
-                } else if (hl == 0) {
-                  // one box {D, HG heads, bs, 1}: smem [bs][HG][D], 1 KB rows for HG = 4
-                  tma_load_4d(tilesK + off, &mapK, &full[st], 0, item.kvh0, 0, bi, pol);
-                  tma_load_4d(tilesV + off, &mapV, &full[st], 0, item.kvh0, 0, bi, pol);
-                }
+              go = 1;
+              if constexpr (NOPS == 2) {
+                // one box {D, HG heads, bs, 1} each for K and V: smem [bs][HG][D]
+                tma_load_4d(tilesK + (size_t)st * stage_bytes, &mapK, &full[st], 0, item.kvh0, 0, bi, pol);
+                tma_load_4d(tilesV + (size_t)st * stage_bytes, &mapV, &full[st], 0, item.kvh0, 0, bi, pol);
               }
-#pragma unroll
-              for (int k = 0; k < WPH; ++k)
-                if (k == w) issued[k] = u + 1;
             }
+          }
+          if constexpr (NOPS > 2) {
+            // tensor-core path: many 128-byte-swizzled 64-column halves per
+            // block, issued by one warp instruction: lane l takes K (l even)
+            // or V (l odd) of head l/2/HALVES, half l/2%HALVES
+            if (__shfl_sync(0xffffffffu, go, 0) && lane < NOPS) {
+              const int rest = lane >> 1;
+              const int hl = rest / HALVES, hh = rest % HALVES;
+              const size_t off = (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes + (size_t)hh * p.bs * 128;
+              unsigned char* dst = ((lane & 1) ? tilesV : tilesK) + off;
+              tma_load_4d(dst, (lane & 1) ? &mapV : &mapK, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
+            }
+          }
+          if (lane == 0 && go) {
+#pragma unroll
+            for (int k = 0; k < WPH; ++k)
+              if (k == w) issued[k] = u + 1;
           }
         }
       }

@@ -45,8 +45,8 @@ constexpr uint32_t kHalf = 16384;      // one 128-row x 64-column bf16 half tile
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = 32768;      // 2 stages x 32 KB
 constexpr uint32_t kOffV = 98304;      // 2 stages x 32 KB
-constexpr uint32_t kOffP = 163840;     // 32 KB
-constexpr uint32_t kOffBar = 196608;
+constexpr uint32_t kOffP = 163840;     // 2 buffers x 32 KB
+constexpr uint32_t kOffBar = 229376;
 constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;   // + barriers + alignment slack
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -60,11 +60,22 @@ struct PrefillParams {
   float qscale;
 };
 
+// Key tile j uses K/V stage j & 1, S buffer j & 1 (TMEM) and P buffer j & 1
+// (shared memory); each buffer has its own barriers, so every wait below is
+// for the next phase of its barrier and a parity can never match a stale one.
 struct Bars {
-  uint64_t q, full_k[2], full_v[2], empty[2], s, p, o, drain;
+  uint64_t q, full_k[2], full_v[2], empty[2], s[2], p[2], pv[2], drain;
   uint32_t tmem_base;
   int abort;
 };
+
+// 2^x with the hardware approximation (flushes subnormal results to zero;
+// the products it feeds are rounded to bf16).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (*abort_flag) return false;
@@ -110,22 +121,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       mbar_init(&bars->full_v[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->s, 1);
-    mbar_init(&bars->p, 128);
-    mbar_init(&bars->o, 1);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(&bars->s[b2], 1);
+      mbar_init(&bars->p[b2], 128);
+      mbar_init(&bars->pv[b2], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 256);
+    tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tO = tmem + 256;             // S buffers at columns 0 and 128
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -166,16 +179,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
           mbar_arrive_expect_tx(&bars->full_k[st], (uint32_t)nvalid * 2u * rows_bytes);
           mbar_arrive_expect_tx(&bars->full_v[st], (uint32_t)nvalid * 2u * rows_bytes);
         }
-        for (int jj = 0; jj < nvalid; ++jj) {
-          const int bi = __shfl_sync(0xffffffffu, blk, jj);
-          if (lane == 0) {
-            unsigned char* kdst = smem + kOffK + st * 2 * kHalf + jj * rows_bytes;
-            unsigned char* vdst = smem + kOffV + st * 2 * kHalf + jj * rows_bytes;
-            tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, bi, pol);
-            tma_load_4d(kdst + kHalf, &mapK, &bars->full_k[st], 64, kvh, 0, bi, pol);
-            tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, bi, pol);
-            tma_load_4d(vdst + kHalf, &mapV, &bars->full_v[st], 64, kvh, 0, bi, pol);
-          }
+        __syncwarp();
+        // lane jj loads block jj of the tile: one warp instruction per operand half
+        if (lane < nvalid) {
+          unsigned char* kdst = smem + kOffK + st * 2 * kHalf + lane * rows_bytes;
+          unsigned char* vdst = smem + kOffV + st * 2 * kHalf + lane * rows_bytes;
+          tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, blk, pol);
+          tma_load_4d(kdst + kHalf, &mapK, &bars->full_k[st], 64, kvh, 0, blk, pol);
+          tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, blk, pol);
+          tma_load_4d(vdst + kHalf, &mapV, &bars->full_v[st], 64, kvh, 0, blk, pol);
         }
         issued = j + 1;
       }
@@ -190,35 +202,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // S_{j+1} = Q K_{j+1}^T is issued before O += P_j V_j, so the tensor core
+    // computes the next scores while the softmax warps work on the current ones.
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
-      if (wait_or_abort(&bars->q, 0, abort_flag)) {
+      auto issue_s = [&](int j) {
+        const uint32_t kb = sbase + kOffK + (j & 1) * 2 * kHalf;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+          umma_bf16(tmem + (j & 1) * 128, sdesc_sw128(sbase + kOffQ + off, 16, 1024),
+                    sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s[j & 1]);
+      };
+      if (wait_or_abort(&bars->q, 0, abort_flag) && wait_or_abort(&bars->full_k[0], 0, abort_flag)) {
         tc_fence_after();
+        issue_s(0);
         for (int j = 0; j < nt; ++j) {
           const int st = j & 1;
-          const uint32_t u = (uint32_t)(j >> 1);
-          if (!wait_or_abort(&bars->full_k[st], u & 1u, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t kb = sbase + kOffK + st * 2 * kHalf;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-            umma_bf16(tS, sdesc_sw128(sbase + kOffQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
-                      kk > 0 ? 1u : 0u);
+          const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+          if (j + 1 < nt) {
+            // S buffer (j+1)&1 was read by the softmax of tile j-1, whose P
+            // this thread waited for in the previous round
+            if (!wait_or_abort(&bars->full_k[(j + 1) & 1], (uint32_t)((j + 1) >> 1) & 1u, abort_flag)) break;
+            tc_fence_after();
+            issue_s(j + 1);
           }
-          umma_commit(&bars->s);
-          if (!wait_or_abort(&bars->p, (uint32_t)j & 1u, abort_flag)) break;
-          if (!wait_or_abort(&bars->full_v[st], u & 1u, abort_flag)) break;
+          if (!wait_or_abort(&bars->p[st], ph, abort_flag)) break;
+          if (!wait_or_abort(&bars->full_v[st], ph, abort_flag)) break;
           tc_fence_after();
           const uint32_t vb = sbase + kOffV + st * 2 * kHalf;
+          const uint32_t pb = sbase + kOffP + st * 2 * kHalf;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t poff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-            umma_bf16(tO, sdesc_sw128(sbase + kOffP + poff, 16, 1024),
-                      sdesc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024), idO, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(tO, sdesc_sw128(pb + poff, 16, 1024), sdesc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024),
+                      idO, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&bars->o);
+          umma_commit(&bars->pv[st]);
           umma_commit(&bars->empty[st]);
         }
       }
@@ -239,51 +262,68 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
 
     for (int j = 0; j < nt && live; ++j) {
       const int st = j & 1;
-      const uint32_t u = (uint32_t)(j >> 1);
+      const uint32_t ph = (uint32_t)(j >> 1) & 1u;
       const int k0 = j * kTile;
-      bool ok = wait_or_abort(&bars->s, (uint32_t)j & 1u, abort_flag);
+      bool ok = wait_or_abort(&bars->s[st], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
       tc_fence_after();
       float s[kTile];
+      {
+        uint32_t v[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + lane_off + c * 32, v);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + st * 128 + lane_off + c * 32, v[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-      }
-      float mx = -INFINITY;
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        const float x = (k0 + c <= pos) ? s[c] * p.qscale : -INFINITY;
-        s[c] = x;
-        mx = fmaxf(mx, x);
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
       }
+      // raw scores; the causal mask only bites on tiles reaching past this row.
+      // Eight independent partial maxima keep the dependency chains short.
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+      if (k0 + kTile - 1 <= pos) {
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) {
+          s[c] = (k0 + c <= pos) ? s[c] : -INFINITY;
+          mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        }
+      }
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      mx *= p.qscale;                                     // scale > 0 (checked by the host)
       const bool need = mx > m_ref + kRescaleThreshold;   // false while mx is -inf
       const float alpha = need ? exp2f(m_ref - mx) : 1.f; // m_ref = -inf gives 0
       if (need) m_ref = mx;
-      if (j > 0) {
-        ok = wait_or_abort(&bars->o, (uint32_t)(j - 1) & 1u, abort_flag);
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled
+        ok = wait_or_abort(&bars->pv[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tO + lane_off + c * 32, v);
-            tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + lane_off + c * 32, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, v);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(tO + lane_off + c * 32, v);
         }
+        tmem_st_wait();
       }
       lsum *= alpha;
+      if (j >= 2) {
+        // P buffer st was last read by P_{j-2} V_{j-2}
+        ok = wait_or_abort(&bars->pv[st], (uint32_t)((j - 2) >> 1) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
+      }
       // V rows at keys >= L hold no context: zero them once the tile has landed
       if (k0 + r >= L) {
-        ok = wait_or_abort(&bars->full_v[st], u & 1u, abort_flag);
+        ok = wait_or_abort(&bars->full_v[st], ph, abort_flag);
         if (ok) {
           uint4 z = make_uint4(0, 0, 0, 0);
           unsigned char* vrow = smem + kOffV + st * 2 * kHalf + r * 128;
@@ -294,33 +334,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
           }
         }
       }
-      // P = exp2(s - m_ref) as bf16, written in the 128-byte-swizzled K-major layout
-      unsigned char* prow = smem + kOffP + r * 128;
+      // P = exp2(scale*s - m_ref) as bf16, in the 128-byte-swizzled K-major layout
+      const float negm = m_ref == -INFINITY ? 0.f : -m_ref;   // all-masked rows: every s is -inf
+      unsigned char* prow = smem + kOffP + st * 2 * kHalf + r * 128;
+      float ls8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float x0 = s[ch * 8 + 2 * e], x1 = s[ch * 8 + 2 * e + 1];
-          const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_ref);
-          const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_ref);
+          const float p0 = ex2_approx(fmaf(s[ch * 8 + 2 * e], p.qscale, negm));
+          const float p1 = ex2_approx(fmaf(s[ch * 8 + 2 * e + 1], p.qscale, negm));
           const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-          lsum += __low2float(pk) + __high2float(pk);
+          ls8[(2 * e) & 7] += __low2float(pk);
+          ls8[(2 * e + 1) & 7] += __high2float(pk);
           w[e] = *reinterpret_cast<const uint32_t*>(&pk);
         }
         const int half = ch >> 3, chunk = ch & 7;
         *reinterpret_cast<uint4*>(prow + half * kHalf + ((chunk ^ (r & 7)) << 4)) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
+      lsum += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p);
+      mbar_arrive(&bars->p[st]);
     }
 
     // epilogue: O / l -> bf16 rows
     bool have = nt > 0 && live;
     if (have) {
-      const bool ok = wait_or_abort(&bars->o, (uint32_t)(nt - 1) & 1u, abort_flag);
+      const bool ok = wait_or_abort(&bars->pv[(nt - 1) & 1], (uint32_t)((nt - 1) >> 1) & 1u, abort_flag);
       have = __all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
@@ -354,7 +399,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -382,7 +427,7 @@ extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, c
       !(block_size == 8 || block_size == 16 || block_size == 32))
     return PA_ERR_SHAPE;
   const int G = num_heads / num_kv_heads;
-  if (G > 16 || (128 % G) != 0) return PA_ERR_SHAPE;
+  if (G > 16 || (128 % G) != 0 || !(scale > 0.f)) return PA_ERR_SHAPE;
   if (num_seqs == 0 || num_queries == 0) return PA_OK;
   if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;

@@ -304,6 +304,7 @@ def cow_case(small=False, device="cpu", seed=None, prompts=None):
 
 def prefill_case(small=False, device="cpu", seed=None, prompts=None, Tq=512, prefix=1024,
                  Hq=None, Hkv=None, bs=None, lens=None, nan_fill=True):
+    # (prompts=None: 2 when small, else 64)
     """Chunked-prefill tile: per prompt, a ``prefix``-token paged context
     (or per-prompt ``lens``) whose last ``Tq`` tokens are the query tile
     (their K/V are already in the pool).  q: [P, Tq, Hq, D].  Defaults are the

@@ -59,5 +59,8 @@ def test_host_side_rejections_launch_nothing(pa):
     # split needed but no workspace (4 partitions)
     assert L.pa_decode(fake, fake, fake, fake, fake, 128, fake, 2, 8, 8, 128, 16, 10, 1.0, 512, null, 0, 1,
                        null) == -5
+    # prefill: head_dim 64 and non-positive scale are rejected
+    assert L.pa_prefill_paged(fake, fake, 16, fake, fake, fake, 8, fake, 2, 8, 8, 64, 16, 10, 1.0, 1, null) == -2
+    assert L.pa_prefill_paged(fake, fake, 16, fake, fake, fake, 8, fake, 2, 8, 8, 128, 16, 10, -1.0, 1, null) == -2
     # empty inputs are a no-op success
     assert L.pa_copy_blocks(null, null, null, 0, 10, 16, 2, 64, 1, null) == 0
