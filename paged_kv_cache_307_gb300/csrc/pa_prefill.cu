@@ -39,17 +39,22 @@ namespace {
 __device__ unsigned g_status_prefill;
 
 constexpr int kThreads = 192;          // 6 warps
-constexpr int kTile = 128;             // rows and keys per tile
+constexpr int kRows = 128;             // query rows per tile
+constexpr int kKT = 64;                // keys per tile
 constexpr int kD = 128;
-constexpr uint32_t kHalf = 16384;      // one 128-row x 64-column bf16 half tile
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = 32768;      // 2 stages x 32 KB
-constexpr uint32_t kOffV = 98304;      // 2 stages x 32 KB
-constexpr uint32_t kOffP = 163840;     // 2 buffers x 32 KB
-constexpr uint32_t kOffBar = 229376;
+constexpr uint32_t kQHalf = 16384;     // 128 rows x 64 columns of bf16
+constexpr uint32_t kKVHalf = 8192;     // 64 keys x 64 columns of bf16
+constexpr uint32_t kOffQ = 0;          // Q: 2 halves x 16 KB
+constexpr uint32_t kOffK = 32768;      // K: 2 stages x (2 halves x 8 KB)
+constexpr uint32_t kOffV = 65536;      // V: 2 stages x (2 halves x 8 KB)
+constexpr uint32_t kOffBar = 98304;
 constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;   // + barriers + alignment slack
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// TMEM columns: S buffers at 0 and 64 (fp32, 64 keys each; P overwrites the
+// first 32 columns of its own S buffer as packed bf16), O at 128..255.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;
 
 struct PrefillParams {
   void* out;
@@ -60,9 +65,11 @@ struct PrefillParams {
   float qscale;
 };
 
-// Key tile j uses K/V stage j & 1, S buffer j & 1 (TMEM) and P buffer j & 1
-// (shared memory); each buffer has its own barriers, so every wait below is
-// for the next phase of its barrier and a parity can never match a stale one.
+// Key tile j uses K/V stage j & 1 and S/P buffer j & 1; each has its own
+// barriers.  tcgen05 operations from the MMA thread execute in issue order
+// and a commit arrives only when every earlier one has completed, so P_j can
+// live in S buffer j & 1 until S_{j+2} (issued after P_j V_j) overwrites it,
+// and an S_j completion also proves that P_{j-2} V_{j-2} has completed.
 struct Bars {
   uint64_t q, full_k[2], full_v[2], empty[2], s[2], p[2], pv[2], drain;
   uint32_t tmem_base;
@@ -85,7 +92,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const PrefillParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -112,33 +119,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
   }
   const int pos0 = L - p.Tq + q0;                 // position of the tile's first query
   const int kend = min(L, pos0 + p.QP);           // keys this tile needs: [0, kend)
-  const int nt = kend > 0 ? (kend + kTile - 1) / kTile : 0;
+  const int nt = kend > 0 ? (kend + kKT - 1) / kKT : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->full_k[s], 1);
-      mbar_init(&bars->full_v[s], 1);
-      mbar_init(&bars->empty[s], 1);
-    }
-    for (int b2 = 0; b2 < 2; ++b2) {
-      mbar_init(&bars->s[b2], 1);
-      mbar_init(&bars->p[b2], 128);
-      mbar_init(&bars->pv[b2], 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&bars->full_k[s2], 1);
+      mbar_init(&bars->full_v[s2], 1);
+      mbar_init(&bars->empty[s2], 1);
+      mbar_init(&bars->s[s2], 1);
+      mbar_init(&bars->p[s2], 128);
+      mbar_init(&bars->pv[s2], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
+    tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t tO = tmem + 256;             // S buffers at columns 0 and 128
+  const uint32_t tO = tmem + kColO;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -148,20 +153,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         prefetch_tensormap(&mapQ);
         prefetch_tensormap(&mapK);
         prefetch_tensormap(&mapV);
-        mbar_arrive_expect_tx(&bars->q, 2 * kHalf);
+        mbar_arrive_expect_tx(&bars->q, 2 * kQHalf);
         const uint64_t pol = policy_evict_first();
         tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, q0, b, pol);
-        tma_load_4d(smem + kOffQ + kHalf, &mapQ, &bars->q, 64, kvh * p.G, q0, b, pol);
+        tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, q0, b, pol);
       }
       issued_q = 1;
       const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by other query tiles
       const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
-      const int nbt = kTile / p.bs;
+      const int nbt = kKT / p.bs;
       const uint32_t rows_bytes = (uint32_t)p.bs * 128u;    // one half-box
       for (int j = 0; j < nt; ++j) {
         const int st = j & 1;
         const uint32_t u = (uint32_t)(j >> 1);
-        const int k0 = j * kTile;
+        const int k0 = j * kKT;
         const int nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
         int blk = 0;
         if (lane < nvalid) {
@@ -182,12 +187,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         __syncwarp();
         // lane jj loads block jj of the tile: one warp instruction per operand half
         if (lane < nvalid) {
-          unsigned char* kdst = smem + kOffK + st * 2 * kHalf + lane * rows_bytes;
-          unsigned char* vdst = smem + kOffV + st * 2 * kHalf + lane * rows_bytes;
+          unsigned char* kdst = smem + kOffK + st * 2 * kKVHalf + lane * rows_bytes;
+          unsigned char* vdst = smem + kOffV + st * 2 * kKVHalf + lane * rows_bytes;
           tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, blk, pol);
-          tma_load_4d(kdst + kHalf, &mapK, &bars->full_k[st], 64, kvh, 0, blk, pol);
+          tma_load_4d(kdst + kKVHalf, &mapK, &bars->full_k[st], 64, kvh, 0, blk, pol);
           tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, blk, pol);
-          tma_load_4d(vdst + kHalf, &mapV, &bars->full_v[st], 64, kvh, 0, blk, pol);
+          tma_load_4d(vdst + kKVHalf, &mapV, &bars->full_v[st], 64, kvh, 0, blk, pol);
         }
         issued = j + 1;
       }
@@ -205,15 +210,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     // S_{j+1} = Q K_{j+1}^T is issued before O += P_j V_j, so the tensor core
     // computes the next scores while the softmax warps work on the current ones.
     if (lane == 0 && nt > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      constexpr uint32_t idS = idesc_bf16_f32(kRows, kKT, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(kRows, kD, false, true);
       auto issue_s = [&](int j) {
-        const uint32_t kb = sbase + kOffK + (j & 1) * 2 * kHalf;
+        const uint32_t kb = sbase + kOffK + (j & 1) * 2 * kKVHalf;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-          umma_bf16(tmem + (j & 1) * 128, sdesc_sw128(sbase + kOffQ + off, 16, 1024),
-                    sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem + (j & 1) * kKT,
+                    sdesc_sw128(sbase + kOffQ + (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u, 16, 1024),
+                    sdesc_sw128(kb + (uint32_t)(kk >> 2) * kKVHalf + (uint32_t)(kk & 3) * 32u, 16, 1024), idS,
+                    kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s[j & 1]);
       };
@@ -224,8 +230,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
           const int st = j & 1;
           const uint32_t ph = (uint32_t)(j >> 1) & 1u;
           if (j + 1 < nt) {
-            // S buffer (j+1)&1 was read by the softmax of tile j-1, whose P
-            // this thread waited for in the previous round
             if (!wait_or_abort(&bars->full_k[(j + 1) & 1], (uint32_t)((j + 1) >> 1) & 1u, abort_flag)) break;
             tc_fence_after();
             issue_s(j + 1);
@@ -233,13 +237,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
           if (!wait_or_abort(&bars->p[st], ph, abort_flag)) break;
           if (!wait_or_abort(&bars->full_v[st], ph, abort_flag)) break;
           tc_fence_after();
-          const uint32_t vb = sbase + kOffV + st * 2 * kHalf;
-          const uint32_t pb = sbase + kOffP + st * 2 * kHalf;
+          const uint32_t vb = sbase + kOffV + st * 2 * kKVHalf;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t poff = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-            umma_bf16(tO, sdesc_sw128(pb + poff, 16, 1024), sdesc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024),
-                      idO, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kKT / 16; ++kk) {
+            // A = P (bf16 pairs in S buffer st, 8 columns per 16 keys); B = V rows kk*16.., MN-major
+            umma_bf16_ts(tO, tmem + st * kKT + kk * 8, sdesc_sw128(vb + (uint32_t)kk * 2048u, kKVHalf, 1024), idO,
+                         (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&bars->pv[st]);
           umma_commit(&bars->empty[st]);
@@ -263,18 +266,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     for (int j = 0; j < nt && live; ++j) {
       const int st = j & 1;
       const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-      const int k0 = j * kTile;
+      const int k0 = j * kKT;
       bool ok = wait_or_abort(&bars->s[st], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
       tc_fence_after();
-      float s[kTile];
+      float s[kKT];
       {
-        uint32_t v[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + st * 128 + lane_off + c * 32, v[c]);
+        uint32_t v[2][32];
+        tmem_ld32(tmem + st * kKT + lane_off, v[0]);
+        tmem_ld32(tmem + st * kKT + 32 + lane_off, v[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
       }
@@ -283,12 +286,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-      if (k0 + kTile - 1 <= pos) {
+      if (k0 + kKT - 1 <= pos) {
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        for (int c = 0; c < kKT; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
       } else {
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
+        for (int c = 0; c < kKT; ++c) {
           s[c] = (k0 + c <= pos) ? s[c] : -INFINITY;
           mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
         }
@@ -316,48 +319,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         tmem_st_wait();
       }
       lsum *= alpha;
-      if (j >= 2) {
-        // P buffer st was last read by P_{j-2} V_{j-2}
-        ok = wait_or_abort(&bars->pv[st], (uint32_t)((j - 2) >> 1) & 1u, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
-      }
       // V rows at keys >= L hold no context: zero them once the tile has landed
-      if (k0 + r >= L) {
+      if (r < kKT && k0 + r >= L) {
         ok = wait_or_abort(&bars->full_v[st], ph, abort_flag);
         if (ok) {
           uint4 z = make_uint4(0, 0, 0, 0);
-          unsigned char* vrow = smem + kOffV + st * 2 * kHalf + r * 128;
+          unsigned char* vrow = smem + kOffV + st * 2 * kKVHalf + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             *reinterpret_cast<uint4*>(vrow + c * 16) = z;
-            *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = z;
+            *reinterpret_cast<uint4*>(vrow + kKVHalf + c * 16) = z;
           }
+          fence_proxy_async_smem();
         }
       }
-      // P = exp2(scale*s - m_ref) as bf16, in the 128-byte-swizzled K-major layout
+      // P = exp2(scale*s - m_ref) as bf16 pairs, written over this S buffer
       const float negm = m_ref == -INFINITY ? 0.f : -m_ref;   // all-masked rows: every s is -inf
-      unsigned char* prow = smem + kOffP + st * 2 * kHalf + r * 128;
+      uint32_t pw[32];
       float ls8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(fmaf(s[ch * 8 + 2 * e], p.qscale, negm));
-          const float p1 = ex2_approx(fmaf(s[ch * 8 + 2 * e + 1], p.qscale, negm));
-          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-          ls8[(2 * e) & 7] += __low2float(pk);
-          ls8[(2 * e + 1) & 7] += __high2float(pk);
-          w[e] = *reinterpret_cast<const uint32_t*>(&pk);
-        }
-        const int half = ch >> 3, chunk = ch & 7;
-        *reinterpret_cast<uint4*>(prow + half * kHalf + ((chunk ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2_approx(fmaf(s[2 * c], p.qscale, negm));
+        const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.qscale, negm));
+        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+        ls8[(2 * c) & 7] += __low2float(pk);
+        ls8[(2 * c + 1) & 7] += __high2float(pk);
+        pw[c] = *reinterpret_cast<const uint32_t*>(&pk);
       }
       lsum += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      fence_proxy_async_smem();
+      tmem_st32(tmem + st * kKT + lane_off, pw);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p[st]);
     }
@@ -399,7 +392,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
