@@ -40,6 +40,9 @@ WORKLOAD_TEXT = {
     "c4": "bf16 GQA decode: 32/8 heads, head_dim 128, block_size 16, batch 256, context U[1024,32768], "
           "split-K 512; plus reshape_and_cache of 256 new tokens",
     "c4b32": "as c4 with block_size 32",
+    "swap": "preemption swap of the c2 pool layout (bf16, 32 heads, head_dim 128, block_size 16): "
+            "4096 scattered blocks (1.07 GB of K+V) out to page-locked host memory and back into "
+            "other scattered device blocks",
     "c5prefill": "bf16 GQA 32/8 causal chunked-prefill tile: 64 prompts, 512 queries at positions 512..1023 "
                  "over a 1024-token paged context (block_size 16), tensor cores",
     "c5": "bf16 GQA decode 32/8, 64 prompts x 8 samples sharing 1024-token prompts + private tails U[0,256]; "
@@ -249,6 +252,49 @@ def run_reference_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+def _swap_sample(nblk, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    shape = (nblk, 16, 32, 128)
+    k = rng.integers(0, 1 << 16, size=(2 * nblk,) + shape[1:], dtype=np.uint16)
+    v = rng.integers(0, 1 << 16, size=(2 * nblk,) + shape[1:], dtype=np.uint16)
+    hk, hv = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    perm = rng.permutation(2 * nblk)
+    out_pairs = np.stack([perm[:nblk], np.arange(nblk)], 1)
+    in_pairs = np.stack([np.arange(nblk), perm[nblk:]], 1)
+    return k, v, hk, hv, out_pairs, in_pairs
+
+
+def swap_cpu_once(sample):
+    import oracle
+    k, v, hk, hv, out_pairs, in_pairs = sample
+    hk, hv = oracle.swap_blocks(hk, hv, k, v, out_pairs)
+    return oracle.swap_blocks(k, v, hk, hv, in_pairs)
+
+
+def run_reference_swap(args):
+    """Oracle swap on one host core: each step swaps a 64-block sample of the
+    swap workload out and back in (the oracle copies whole pools)."""
+    sample = _swap_sample(64, 5)
+    moved = 2 * 2 * 64 * 16 * 32 * 128 * 2
+    for _ in range(args.warmup):
+        swap_cpu_once(sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        swap_cpu_once(sample)
+    dt = time.perf_counter() - t0
+    val = moved * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": "KV block swap GB/s (device <-> page-locked host, both directions)",
+            "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": "swap: " + WORKLOAD_TEXT["swap"], "sample": "64 blocks out and back per step"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d steps of 64 blocks out and back" % args.steps},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle timed on one host core: each step is one (sequence, KV head)
     slice of the workload (append + decode), cycling through a 16-sequence
@@ -257,6 +303,8 @@ def run_reference(args, rank, world):
         return
     if args.workload == "c5prefill":
         return run_reference_prefill(args)
+    if args.workload == "swap":
+        return run_reference_swap(args)
     tasks, nbytes = _cpu_tasks(args.workload, 16, seed=12345)
     for i in range(args.warmup):
         _oracle_slice(tasks[i % len(tasks)])
@@ -393,6 +441,104 @@ def run_prefill(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args, rank, world, local_rank):
+    """Swap-out then swap-in of 4096 blocks (pa_swap_blocks both ways).
+    Metric: GB/s of K/V bytes moved over the host link (both directions).
+    The copy engine moving the same bytes as one contiguous transfer each
+    way is timed beside it as the link's measured rate."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_307_gb300 import build as B
+    B.build()
+    from paged_kv_cache_307_gb300 import _lib as pa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    NB, bs, H, D, n = 8192, 16, 32, 128, args.batch or 4096
+    g = torch.Generator(device=dev).manual_seed(4242 + rank)
+    k = torch.randn(NB, bs, H, D, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn(NB, bs, H, D, device=dev, generator=g).to(torch.bfloat16)
+    hk = torch.empty((n, bs, H, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(7 + rank)
+    perm = rng.permutation(NB)
+    out_pairs = torch.from_numpy(np.stack([perm[:n], np.arange(n)], 1)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(n), perm[n:2 * n] if 2 * n <= NB else perm[:n]], 1)).to(dev)
+    block_bytes = bs * H * D * 2
+    moved = 2 * 2 * n * block_bytes                      # K and V, out and back
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa.swap_blocks(hk, hv, k, v, out_pairs)
+        pa.swap_blocks(k, v, hk, hv, in_pairs)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pa.last_error() == 0
+    K = min(args.steps, 200)
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    sampler = ClockSampler(int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].isdigit()
+                           else local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    e[0].record(stream)
+    for _ in range(K):
+        step()
+    e[1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert pa.last_error() == 0
+    ms = e[0].elapsed_time(e[1]) / K
+    value = world * moved / (ms / 1e3) / 1e9
+    # copy engine, same bytes, contiguous, both directions
+    flat_d = k[:n].view(-1)
+    flat_h = hk.view(-1)
+    for _ in range(3):
+        flat_h.copy_(flat_d, non_blocking=True)
+        flat_d.copy_(flat_h, non_blocking=True)
+    torch.cuda.synchronize()
+    Kc = min(K, 50)
+    e[0].record(stream)
+    for _ in range(Kc):
+        for _ in range(2):                               # K and V
+            flat_h.copy_(flat_d, non_blocking=True)
+            flat_d.copy_(flat_h, non_blocking=True)
+    e[1].record(stream)
+    torch.cuda.synchronize()
+    ce_gbs = moved / (e[0].elapsed_time(e[1]) / Kc / 1e3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": "KV block swap GB/s (device <-> page-locked host, both directions)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "swap: " + WORKLOAD_TEXT["swap"], "blocks": n, "block_bytes_kv": 2 * block_bytes,
+                   "bytes_per_step": moved, "l2": "1.07 GB each way, larger than L2; no flush"},
+        "roofline": {"bound": "host link", "achieved": round(value, 2), "peak": round(ce_gbs, 2), "unit": "GB/s",
+                     "frac": round(value / ce_gbs, 4), "traffic": None,
+                     "kernel": "swap_blocks_kernel (copies over NVLink-C2C from SM loads/stores)",
+                     "peak_source": "copy engine moving the same bytes contiguously, measured in this run"},
+        "e2e": {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": moved // 2,
+                "d2h_bytes_per_step": moved // 2, "note": "the swap is itself the host transfer"},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        sample = _swap_sample(64, 5)
+        t0, reps = time.perf_counter(), 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            swap_cpu_once(sample)
+            reps += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(reps * 2 * 2 * 64 * block_bytes / dt / 1e9, 4), "unit": "GB/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": "%d repetitions of 64 blocks out and back (numpy copies)" % reps}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -465,6 +611,37 @@ def run_ours(args, rank, world, local_rank):
     step_s = total_ms / 1e3 / K
     value = world * step_bytes / step_s / 1e9
 
+    # the same step captured once as a CUDA graph and replayed K times
+    graph_line = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            append()
+            decode()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            append()
+            decode()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        for _ in range(K):
+            graph.replay()
+        gb.record(stream)
+        torch.cuda.synchronize()
+        assert pa.last_error() == 0, "device-detected error in graph replay"
+        g_ms = ga.elapsed_time(gb) / K
+        graph_line = {"ms_per_step": round(g_ms, 5), "value": round(world * step_bytes / (g_ms / 1e3) / 1e9, 2),
+                      "unit": "GB/s", "steps": K, "note": "append + decode captured once, replayed per step"}
+        del graph
+    except RuntimeError as exc:
+        graph_line = {"error": str(exc).splitlines()[0][:200]}
+
     # end to end through the public API: pinned host inputs in, result out
     host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "key", "value", "slot_mapping",
                                                              "block_tables", "context_lens")}
@@ -529,6 +706,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h, "steps": Ke, "ms_per_step": round(e2e_ms / Ke, 5)},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
+        "graph": graph_line,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
@@ -554,6 +732,8 @@ def main():
     try:
         if args.workload == "c5prefill":
             run_prefill(args, rank, world, local_rank)
+        elif args.workload == "swap":
+            run_swap(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -130,6 +130,31 @@ int pa_decode(void* out, const void* query,
               pa_dtype dtype, void* stream);
 
 /*
+ * Swap blocks between two pools (preemption by swapping).  [KVS] §19.2.6:
+ * a preempted request's KV cache can be moved out to CPU memory and moved
+ * back when GPU memory frees up; [OS] §九 names the same swap-out.  For each
+ * pair i, block pairs[2i+1] of the destination pool (dst_k, dst_v) becomes a
+ * byte-exact copy of block pairs[2i] of the source pool (src_k, src_v), all
+ * slots and heads.  Both pools have the [num_blocks, block_size,
+ * num_kv_heads, head_dim] layout; their block counts may differ.
+ *
+ *   dst_*, src_*  device-accessible addresses: device memory, or page-locked
+ *                 host memory the device can address (on GB300 such host
+ *                 memory is reached over NVLink-C2C by the copy kernel itself,
+ *                 so no staging buffer is needed)
+ *   pairs         [num_pairs, 2] int64 (src block, dst block), device memory;
+ *                 destination blocks distinct, pools not overlapping
+ *
+ * A pair naming a block outside its pool is skipped and sets
+ * PA_DEV_BAD_BLOCK.  num_pairs == 0 launches nothing.
+ */
+int pa_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks,
+                   const void* src_k, const void* src_v, int src_num_blocks,
+                   const int64_t* pairs, int num_pairs,
+                   int block_size, int num_kv_heads, int head_dim,
+                   pa_dtype dtype, void* stream);
+
+/*
  * Decode that allocates nothing and takes no workspace.  This entry point
  * has no counterpart on the paged-attention pages; it exists for callers
  * that cannot allocate device memory at the point of the call — for example

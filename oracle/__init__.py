@@ -40,5 +40,5 @@ from .attention import (  # noqa: F401
     paged_decode_split,
     paged_prefill,
 )
-from .cache_ops import reshape_and_cache, copy_blocks  # noqa: F401
+from .cache_ops import reshape_and_cache, copy_blocks, swap_blocks  # noqa: F401
 from .block_manager import BlockPool, BlockTable, BlockExhausted  # noqa: F401

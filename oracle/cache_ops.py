@@ -50,3 +50,18 @@ def copy_blocks(k_cache, v_cache, pairs):
         kc[int(dst)] = kc[int(src)]
         vc[int(dst)] = vc[int(src)]
     return kc, vc
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs):
+    """Preemption by swapping: block pairs[i, 1] of the destination pool
+    becomes a copy of block pairs[i, 0] of the source pool (whole blocks, K and
+    V).  [KVS] "19.2 KV Cache 系统化管理" §19.2.6 (swap a preempted request's KV
+    cache out to CPU memory and back when memory frees up) and [OS] §九.  The
+    two pools may differ in block count; every pair must name valid blocks and
+    the destination blocks must be distinct."""
+    kc = np.array(dst_k, copy=True)
+    vc = np.array(dst_v, copy=True)
+    for src, dst in np.asarray(pairs).reshape(-1, 2):
+        kc[int(dst)] = src_k[int(src)]
+        vc[int(dst)] = src_v[int(src)]
+    return kc, vc

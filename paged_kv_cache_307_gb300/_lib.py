@@ -41,6 +41,8 @@ lib.pa_copy_blocks.argtypes = [_p, _p, _i64p, _i, _i, _i, _i, _i, _i, _p]
 lib.pa_copy_blocks.restype = _i
 lib.pa_prefill_paged.argtypes = [_p, _p, _i, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
 lib.pa_prefill_paged.restype = _i
+lib.pa_swap_blocks.argtypes = [_p, _p, _i, _p, _p, _i, _i64p, _i, _i, _i, _i, _i, _p]
+lib.pa_swap_blocks.restype = _i
 lib.pa_last_error.argtypes = []
 lib.pa_last_error.restype = _i
 lib.pa_strerror.argtypes = [_i]
@@ -156,6 +158,18 @@ def prefill(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=
                                 block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
                                 ctypes.c_float(scale), _dtype(q), _stream(stream)), "pa_prefill_paged")
     return out
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, stream=None):
+    """Block pairs[i,1] of (dst_k, dst_v) becomes a copy of block pairs[i,0]
+    of (src_k, src_v).  Either pool may be pinned host memory."""
+    _contig(dst_k, dst_v, src_k, src_v, pairs)
+    assert pairs.dtype == torch.int64 and pairs.is_cuda
+    assert dst_k.shape[1:] == src_k.shape[1:] and dst_k.dtype == src_k.dtype
+    _, bs, H, D = dst_k.shape
+    _check(lib.pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), dst_k.shape[0], _ptr(src_k), _ptr(src_v), src_k.shape[0],
+                              _ptr(pairs), pairs.shape[0], bs, H, D, _dtype(dst_k), _stream(stream)),
+           "pa_swap_blocks")
 
 
 def last_error():

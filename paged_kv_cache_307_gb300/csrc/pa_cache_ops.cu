@@ -74,6 +74,41 @@ copy_blocks_kernel(unsigned char* __restrict__ k_cache, unsigned char* __restric
   cta_copy16(base + dst * block_bytes + off, base + src * block_bytes + off, (int)(n / 16));
 }
 
+// Coherent 16-byte copy (the source may be page-locked host memory).
+__device__ __forceinline__ void cta_copy16_coherent(unsigned char* __restrict__ dst,
+                                                    const unsigned char* __restrict__ src, int chunks) {
+  int c = threadIdx.x;
+  for (; c + (kUnroll - 1) * kCopyThreads < chunks; c += kUnroll * kCopyThreads) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = *reinterpret_cast<const uint4*>(src + (size_t)(c + u * kCopyThreads) * 16);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) st_v4(dst + (size_t)(c + u * kCopyThreads) * 16, v[u]);
+  }
+  for (; c < chunks; c += kCopyThreads)
+    st_v4(dst + (size_t)c * 16, *reinterpret_cast<const uint4*>(src + (size_t)c * 16));
+}
+
+// grid: (num_pairs, 2, spans).  Block pairs[i,1] of the destination pool
+// becomes a copy of block pairs[i,0] of the source pool.
+__global__ void __launch_bounds__(kCopyThreads)
+swap_blocks_kernel(unsigned char* __restrict__ dst_k, unsigned char* __restrict__ dst_v,
+                   const unsigned char* __restrict__ src_k, const unsigned char* __restrict__ src_v,
+                   const int64_t* __restrict__ pairs, long long src_blocks, long long dst_blocks,
+                   long long block_bytes, int span_bytes) {
+  const long long src = pairs[2 * (size_t)blockIdx.x];
+  const long long dst = pairs[2 * (size_t)blockIdx.x + 1];
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(&g_status_cache, PA_DEV_BAD_BLOCK);
+    return;
+  }
+  const long long off = (long long)blockIdx.z * span_bytes;
+  const long long n = block_bytes - off < span_bytes ? block_bytes - off : span_bytes;
+  unsigned char* d = (blockIdx.y == 0 ? dst_k : dst_v) + dst * block_bytes + off;
+  const unsigned char* s = (blockIdx.y == 0 ? src_k : src_v) + src * block_bytes + off;
+  cta_copy16_coherent(d, s, (int)(n / 16));
+}
+
 }  // namespace
 
 unsigned fetch_status_cache_ops() {
@@ -123,4 +158,24 @@ extern "C" int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs
   copy_blocks_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
       (unsigned char*)k_cache, (unsigned char*)v_cache, pairs, num_blocks, block_bytes, span);
   return ck(cudaGetLastError(), "launch copy_blocks_kernel") ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" int pa_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks, const void* src_k, const void* src_v,
+                              int src_num_blocks, const int64_t* pairs, int num_pairs, int block_size,
+                              int num_kv_heads, int head_dim, pa_dtype dtype, void* stream) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (num_pairs < 0 || dst_num_blocks <= 0 || src_num_blocks <= 0 || num_kv_heads <= 0 ||
+      !supported_head_dim(head_dim) || !supported_block_size(block_size))
+    return PA_ERR_SHAPE;
+  if (num_pairs == 0) return PA_OK;
+  if (!dst_k || !dst_v || !src_k || !src_v || !pairs) return PA_ERR_NULL;
+  if (!aligned16(dst_k) || !aligned16(dst_v) || !aligned16(src_k) || !aligned16(src_v)) return PA_ERR_ALIGN;
+  const long long block_bytes = (long long)block_size * num_kv_heads * head_dim * elem_bytes(dtype);
+  const int span = 32 * 1024;
+  const unsigned spans = (unsigned)((block_bytes + span - 1) / span);
+  dim3 grid((unsigned)num_pairs, 2, spans);
+  swap_blocks_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
+      (unsigned char*)dst_k, (unsigned char*)dst_v, (const unsigned char*)src_k, (const unsigned char*)src_v, pairs,
+      src_num_blocks, dst_num_blocks, block_bytes, span);
+  return ck(cudaGetLastError(), "launch swap_blocks_kernel") ? PA_OK : PA_ERR_CUDA;
 }

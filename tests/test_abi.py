@@ -62,5 +62,10 @@ def test_host_side_rejections_launch_nothing(pa):
     # prefill: head_dim 64 and non-positive scale are rejected
     assert L.pa_prefill_paged(fake, fake, 16, fake, fake, fake, 8, fake, 2, 8, 8, 64, 16, 10, 1.0, 1, null) == -2
     assert L.pa_prefill_paged(fake, fake, 16, fake, fake, fake, 8, fake, 2, 8, 8, 128, 16, 10, -1.0, 1, null) == -2
+    # swap: null source pool, misaligned destination, unsupported block size
+    assert L.pa_swap_blocks(fake, fake, 4, null, fake, 10, fake, 2, 16, 2, 64, 1, null) == -1
+    assert L.pa_swap_blocks(odd, fake, 4, fake, fake, 10, fake, 2, 16, 2, 64, 1, null) == -4
+    assert L.pa_swap_blocks(fake, fake, 4, fake, fake, 10, fake, 2, 12, 2, 64, 1, null) == -2
     # empty inputs are a no-op success
     assert L.pa_copy_blocks(null, null, null, 0, 10, 16, 2, 64, 1, null) == 0
+    assert L.pa_swap_blocks(null, null, 4, null, null, 10, null, 0, 16, 2, 64, 1, null) == 0

@@ -82,6 +82,76 @@ def test_copy_blocks_fp32_and_bad_pair(pa):
     assert np.array_equal(bits(k), exp_k) and np.array_equal(bits(v), exp_v)
 
 
+@pytest.mark.parametrize("dtype,bs,H,D", [("bf16", 16, 8, 128), ("f32", 16, 2, 64), ("bf16", 32, 8, 128),
+                                         ("bf16", 4, 1, 32)])
+def test_swap_out_to_pinned_host_and_back(pa, dtype, bs, H, D):
+    """Preempt: blocks of a device pool go to a page-locked host pool and come
+    back into different device blocks; byte-exact both ways, and decode over
+    the remapped table gives bit-identical output."""
+    dt = W.DTYPES[dtype]
+    g = torch.Generator(device="cuda").manual_seed(bs * D)
+    NB, NH = 40, 12
+    dev_k = torch.randn(NB, bs, H, D, device="cuda", generator=g).to(dt)
+    dev_v = torch.randn(NB, bs, H, D, device="cuda", generator=g).to(dt)
+    host_k = torch.zeros(NH, bs, H, D, dtype=dt).pin_memory()
+    host_v = torch.zeros(NH, bs, H, D, dtype=dt).pin_memory()
+    out_pairs = torch.tensor([[3, 0], [17, 5], [39, 11], [8, 2]], dtype=torch.int64)
+    exp_hk, exp_hv = oracle.swap_blocks(bits(host_k), bits(host_v), bits(dev_k), bits(dev_v), out_pairs.numpy())
+    pa.swap_blocks(host_k, host_v, dev_k, dev_v, out_pairs.cuda())
+    torch.cuda.synchronize()
+    assert pa.last_error() == 0
+    assert np.array_equal(bits(host_k), exp_hk) and np.array_equal(bits(host_v), exp_hv)
+    # swap in to other device blocks of a second pool
+    back = torch.tensor([[0, 21], [5, 22], [11, 23], [2, 24]], dtype=torch.int64)
+    new_k, new_v = torch.zeros_like(dev_k), torch.zeros_like(dev_v)
+    exp_k, exp_v = oracle.swap_blocks(bits(new_k), bits(new_v), exp_hk, exp_hv, back.numpy())
+    pa.swap_blocks(new_k, new_v, host_k, host_v, back.cuda())
+    assert pa.last_error() == 0
+    assert np.array_equal(bits(new_k), exp_k) and np.array_equal(bits(new_v), exp_v)
+    for (s, _), (_, d) in zip(out_pairs.tolist(), back.tolist()):
+        assert np.array_equal(bits(new_k)[d], bits(dev_k)[s]) and np.array_equal(bits(new_v)[d], bits(dev_v)[s])
+
+
+def test_swap_restores_decode_bit_identically(pa):
+    c = _cuda_case("c4", small=True)
+    pa.reshape_and_cache(c.key, c.value, c.slot_mapping, c.k_cache, c.v_cache)
+    out1 = gpu_decode(c, append=False)
+    # swap sequence 0 out, wipe its device blocks, swap it back in elsewhere
+    L = int(c.context_lens[0])
+    n = -(-L // c.spec.bs)
+    blocks = c.block_tables[0, :n].long()
+    hk = torch.empty((n,) + c.k_cache.shape[1:], dtype=c.k_cache.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    ar = torch.arange(n, device="cuda")
+    pa.swap_blocks(hk, hv, c.k_cache, c.v_cache, torch.stack([blocks, ar], 1).contiguous())
+    c.k_cache[blocks] = float("nan")
+    c.v_cache[blocks] = float("nan")
+    k = torch.cat([c.k_cache, torch.empty((n,) + c.k_cache.shape[1:], dtype=c.k_cache.dtype, device="cuda")])
+    v = torch.cat([c.v_cache, torch.empty_like(k[c.num_blocks:])])
+    new = ar + c.num_blocks
+    pa.swap_blocks(k, v, hk, hv, torch.stack([ar, new], 1).contiguous())
+    t = c.block_tables.clone()
+    t[t == c.num_blocks] = k.shape[0]
+    t[0, :n] = new.int()
+    c.k_cache, c.v_cache, c.block_tables = k, v, t.contiguous()
+    out2 = gpu_decode(c, append=False)
+    assert pa.last_error() == 0
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_swap_bad_pair_is_flagged_and_skipped(pa):
+    k = torch.randn(6, 16, 2, 64, device="cuda")
+    v = torch.randn(6, 16, 2, 64, device="cuda")
+    hk = torch.zeros(3, 16, 2, 64).pin_memory()
+    hv = torch.zeros(3, 16, 2, 64).pin_memory()
+    pa.swap_blocks(hk, hv, k, v, torch.tensor([[1, 0], [2, 3], [9, 1]], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert pa.last_error() == pa.DEV_BAD_BLOCK
+    exp_k, exp_v = oracle.swap_blocks(np.zeros((3, 16, 2, 64), np.float32), np.zeros((3, 16, 2, 64), np.float32),
+                                      bits(k).view(np.float32), bits(v).view(np.float32), np.array([[1, 0]]))
+    assert np.array_equal(hk.numpy(), exp_k) and np.array_equal(hv.numpy(), exp_v)
+
+
 # ------------------------------------------------------------------ decode, small
 
 @pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c4b32", "c5"])

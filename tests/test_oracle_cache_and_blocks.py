@@ -136,3 +136,20 @@ def test_copy_blocks_is_bit_identical_and_local():
     for blk in range(10):
         if blk not in (7, 8, 9):
             assert np.array_equal(k2[blk], k[blk]) and np.array_equal(v2[blk], v[blk])
+
+
+def test_swap_out_and_back_is_identity():
+    rng = np.random.default_rng(3)
+    dev_k = rng.integers(0, 1 << 16, size=(12, 4, 2, 8), dtype=np.uint16)
+    dev_v = rng.integers(0, 1 << 16, size=(12, 4, 2, 8), dtype=np.uint16)
+    host_k = np.zeros((5, 4, 2, 8), np.uint16)
+    host_v = np.zeros((5, 4, 2, 8), np.uint16)
+    out_pairs = np.array([[3, 0], [7, 4], [11, 2]])
+    hk, hv = oracle.swap_blocks(host_k, host_v, dev_k, dev_v, out_pairs)
+    for s, d in out_pairs:
+        assert np.array_equal(hk[d], dev_k[s]) and np.array_equal(hv[d], dev_v[s])
+    assert not hk[1].any() and not hk[3].any()           # untouched host blocks
+    # back into fresh device blocks, then a table remap sees the same data
+    back = np.array([[0, 9], [4, 10], [2, 1]])
+    k2, v2 = oracle.swap_blocks(np.zeros_like(dev_k), np.zeros_like(dev_v), hk, hv, back)
+    assert np.array_equal(k2[9], dev_k[3]) and np.array_equal(v2[10], dev_v[7]) and np.array_equal(k2[1], dev_k[11])
