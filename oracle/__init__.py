@@ -15,6 +15,7 @@ Pages this oracle restates (cited by title and section everywhere below):
 * [OS]   "LLM 推理引擎的内存管理与调度：PagedAttention、Prefix Cache 与
   Continuous Batching" (zhouzhq2021.github.io): §三 block-table diagram,
   §四 reference counts and copy-on-write, §8.1 chunked prefill.
+  §19.2.4 KV cache quantisation (per-token scaled FP8, ``quant.py``).
 * [SCH]  "KV Cache、PagedAttention 与调度器" (gongshangzheng.github.io):
   the 13B-per-sequence KV size claim.
 
@@ -41,4 +42,12 @@ from .attention import (  # noqa: F401
     paged_prefill,
 )
 from .cache_ops import reshape_and_cache, copy_blocks, swap_blocks  # noqa: F401
+from .quant import (  # noqa: F401
+    e4m3_decode,
+    e4m3_encode,
+    quantize_token,
+    dequantize,
+    reshape_and_cache_fp8,
+    paged_decode_fp8,
+)
 from .block_manager import BlockPool, BlockTable, BlockExhausted  # noqa: F401
