@@ -40,6 +40,9 @@ WORKLOAD_TEXT = {
     "c4": "bf16 GQA decode: 32/8 heads, head_dim 128, block_size 16, batch 256, context U[1024,32768], "
           "split-K 512; plus reshape_and_cache of 256 new tokens",
     "c4b32": "as c4 with block_size 32",
+    "c2fp8": "as c2 over an e4m3 K/V pool with per-token fp32 scales (codes + scales read per token); "
+             "append quantises the 64 new tokens",
+    "c4fp8": "as c4 over an e4m3 K/V pool with per-token fp32 scales; append quantises the 256 new tokens",
     "swap": "preemption swap of the c2 pool layout (bf16, 32 heads, head_dim 128, block_size 16): "
             "4096 scattered blocks (1.07 GB of K+V) out to page-locked host memory and back into "
             "other scattered device blocks",
@@ -159,6 +162,43 @@ def _oracle_slice(task):
     return oracle.paged_decode(_widen(q)[None], k, v, table, np.array([L]), scale)
 
 
+def _oracle_seq_fp8(task):
+    """One sequence of an e4m3 workload through the oracle: quantise-append
+    the newest token (all heads: the scale is per token), then decode."""
+    import numpy as np
+    import oracle
+    q, kc, vc, ks, vs, L, key, val, slot, scale = task
+    kc, vc, ks, vs = oracle.reshape_and_cache_fp8(_widen(key)[None], _widen(val)[None], np.array([slot]),
+                                                  kc, vc, ks, vs)
+    table = np.arange(kc.shape[0])[None]
+    return oracle.paged_decode_fp8(_widen(q)[None], kc, vc, ks, vs, table, np.array([L]), scale)
+
+
+def _cpu_tasks_fp8(name, nseq, seed):
+    """Per-sequence oracle inputs of an e4m3 workload (compact pools of
+    codes and scales), with their algorithmic bytes."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_307_gb300 import workloads as W
+    c = W.fp8_case(W.decode_case(name[:-3], device="cpu", nan_fill=False, seed=seed, B=nseq))
+    s = c.spec
+    bs = s.bs
+    lens, tables = c.context_lens.numpy(), c.block_tables.numpy()
+    u16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    tasks, nbytes = [], []
+    for b in range(len(lens)):
+        n = -(-int(lens[b]) // bs)
+        blocks = tables[b, :n]
+        slot = int(c.slot_mapping[b])
+        local_slot = int(np.where(blocks == slot // bs)[0][0]) * bs + slot % bs
+        tasks.append((u16(c.q[b]), c.k_cache[blocks].numpy(), c.v_cache[blocks].numpy(),
+                      c.extra["k_scale"][blocks].numpy(), c.extra["v_scale"][blocks].numpy(), int(lens[b]),
+                      u16(c.key[b]), u16(c.value[b]), local_slot, c.scale))
+        nbytes.append(int(lens[b]) * (2 * s.Hkv * s.D + 8) + 2 * s.Hq * s.D * 2 + 4 * n + 4 + 8
+                      + 2 * (s.Hkv * s.D * 2 + s.Hkv * s.D + 4))
+    return tasks, nbytes
+
+
 def _cpu_tasks(name, nseq, seed):
     """Oracle inputs per (sequence, KV head) slice, as bf16 bit patterns with
     the slice's blocks gathered into a compact pool, drawn by the same
@@ -203,21 +243,24 @@ def cpu_baseline(name, seconds):
     repeated until about `seconds` of wall time."""
     cores = os.cpu_count() or 1
     nseq = 16
-    tasks, nbytes = _cpu_tasks(name, nseq, seed=12345)
+    fp8 = name.endswith("fp8")
+    tasks, nbytes = (_cpu_tasks_fp8 if fp8 else _cpu_tasks)(name, nseq, seed=12345)
+    fn = _oracle_seq_fp8 if fp8 else _oracle_slice
     with _pool(cores) as pool:
-        pool.map(_oracle_slice, tasks[:cores])          # worker start-up outside the timing
+        pool.map(fn, tasks[:cores])                     # worker start-up outside the timing
         t0 = time.perf_counter()
         reps = 0
         while True:
-            pool.map(_oracle_slice, tasks, chunksize=4)
+            pool.map(fn, tasks, chunksize=1 if fp8 else 4)
             reps += 1
             if time.perf_counter() - t0 >= seconds:
                 break
         dt = time.perf_counter() - t0
     gbs = reps * sum(nbytes) / dt / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": "%d passes over a %d-sequence sample of workload %s, split into %d (sequence, KV head) "
-                      "slices (append + decode, float64), %.1f s wall" % (reps, nseq, name, len(tasks), dt),
+            "sample": "%d passes over a %d-sequence sample of workload %s, split into %d %s "
+                      "slices (append + decode, float64), %.1f s wall"
+                      % (reps, nseq, name, len(tasks), "sequence" if fp8 else "(sequence, KV head)", dt),
             "seq_steps_per_s": round(reps * nseq / dt, 3)}
 
 
@@ -305,27 +348,30 @@ def run_reference(args, rank, world):
         return run_reference_prefill(args)
     if args.workload == "swap":
         return run_reference_swap(args)
-    tasks, nbytes = _cpu_tasks(args.workload, 16, seed=12345)
+    fp8 = args.workload.endswith("fp8")
+    tasks, nbytes = (_cpu_tasks_fp8 if fp8 else _cpu_tasks)(args.workload, 16, seed=12345)
+    fn = _oracle_seq_fp8 if fp8 else _oracle_slice
     for i in range(args.warmup):
-        _oracle_slice(tasks[i % len(tasks)])
+        fn(tasks[i % len(tasks)])
     t0 = time.perf_counter()
     done = 0.0
     for i in range(args.steps):
-        _oracle_slice(tasks[i % len(tasks)])
+        fn(tasks[i % len(tasks)])
         done += nbytes[i % len(tasks)]
     dt = time.perf_counter() - t0
     step = dt / args.steps
     gbs = done / dt / 1e9
+    unit = "sequence" if fp8 else "(sequence, KV head) slice"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 5), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload],
-                   "sample": "one (sequence, KV head) slice per step"},
+                   "sample": "one %s per step" % unit},
         "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d (sequence, KV head) slices of a 16-sequence sample of workload %s "
-                                   "(append + decode, float64, one thread)" % (args.steps, args.workload)},
+                         "sample": "%d %ss of a 16-sequence sample of workload %s "
+                                   "(append + decode, float64, one thread)" % (args.steps, unit, args.workload)},
         "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -551,9 +597,13 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    spec = W.SPECS[args.workload]
-    case = W.decode_case(args.workload, device=dev, nan_fill=False, seed=spec.seed + 1000 * rank,
-                         B=args.batch or None)
+    fp8 = args.workload.endswith("fp8")
+    base = args.workload[:-3] if fp8 else args.workload
+    spec = W.SPECS[base]
+    case = W.decode_case(base, device=dev, nan_fill=False, seed=spec.seed + 1000 * rank, B=args.batch or None)
+    if fp8:
+        case = W.fp8_case(case)
+        k_scale, v_scale = case.extra["k_scale"], case.extra["v_scale"]
     Bsz, Hq, D = case.q.shape
     ws = pa.alloc_workspace(case.q, case.k_cache, case.block_tables, args.partition)
     out = torch.empty_like(case.q)
@@ -565,12 +615,25 @@ def run_ours(args, rank, world, local_rank):
     app_bytes = W.append_bytes(case)
     step_bytes = dec_bytes + app_bytes
 
-    def append():
-        pa.reshape_and_cache(case.key, case.value, case.slot_mapping, case.k_cache, case.v_cache)
+    def append(key=None, value=None, slots=None):
+        key = case.key if key is None else key
+        value = case.value if value is None else value
+        slots = case.slot_mapping if slots is None else slots
+        if fp8:
+            pa.reshape_and_cache_fp8(key, value, slots, case.k_cache, case.v_cache, k_scale, v_scale)
+        else:
+            pa.reshape_and_cache(key, value, slots, case.k_cache, case.v_cache)
 
-    def decode():
-        pa.decode(out, case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
-                  case.scale, partition_size=args.partition, workspace=ws)
+    def decode(q=None, tables=None, lens=None):
+        q = case.q if q is None else q
+        tables = case.block_tables if tables is None else tables
+        lens = case.context_lens if lens is None else lens
+        if fp8:
+            pa.decode_fp8(out, q, case.k_cache, case.v_cache, k_scale, v_scale, tables, lens, case.scale,
+                          partition_size=args.partition, workspace=ws)
+        else:
+            pa.decode(out, q, case.k_cache, case.v_cache, tables, lens, case.scale,
+                      partition_size=args.partition, workspace=ws)
 
     for _ in range(max(args.warmup, 3)):
         append()
@@ -653,9 +716,8 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         for n in host:
             devb[n].copy_(host[n], non_blocking=True)
-        pa.reshape_and_cache(devb["key"], devb["value"], devb["slot_mapping"], case.k_cache, case.v_cache)
-        pa.decode(out, devb["q"], case.k_cache, case.v_cache, devb["block_tables"], devb["context_lens"],
-                  case.scale, partition_size=args.partition, workspace=ws)
+        append(devb["key"], devb["value"], devb["slot_mapping"])
+        decode(devb["q"], devb["block_tables"], devb["context_lens"])
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -686,11 +748,13 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
-        spec.dtype == "bf16" else "f32", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 K/V, bf16 Q/O, f32 math" if fp8 else ("bf16" if spec.dtype == "bf16" else "f32"),
+        "data": "synthetic",
         "config": {"workload": args.workload + ": " + WORKLOAD_TEXT[args.workload], "batch": Bsz,
                    "num_heads": Hq, "num_kv_heads": spec.Hkv, "head_dim": D, "block_size": spec.bs,
                    "partition_tokens": P, "pool_bytes": 2 * case.k_cache.numel() * case.k_cache.element_size(),
+                   "kv_dtype": "e4m3 + per-token fp32 scales" if fp8 else spec.dtype,
                    "l2": "inputs larger than L2 (K/V pool %.2f GB vs 129 MB L2); no flush"
                          % (2 * case.k_cache.numel() * case.k_cache.element_size() / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",

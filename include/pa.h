@@ -19,7 +19,9 @@
  *  - Pool layout (from [KVS] §19.2.3): k_cache and v_cache are each
  *    [num_blocks, block_size, num_kv_heads, head_dim], row-major, contiguous,
  *    one layer.  Call once per layer for a multi-layer cache.
- *  - Element type: PA_F32 or PA_BF16; K, V, Q and the output share it.
+ *  - Element type: PA_F32 or PA_BF16; K, V, Q and the output share it,
+ *    except for the e4m3 pool calls (pa_reshape_and_cache_fp8,
+ *    pa_decode_fp8), whose pools hold PA_FP8_E4M3 codes with fp32 scales.
  *    Arithmetic is fp32 whatever the storage type; bf16 results are rounded
  *    to nearest even.
  *  - Supported sizes: head_dim in {32, 64, 128}; block_size in {4, 8, 16,
@@ -48,7 +50,11 @@
 extern "C" {
 #endif
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+/* PA_FP8_E4M3 is a storage type for K/V pools only: 8-bit e4m3 codes (4
+ * exponent bits with bias 7, 3 mantissa bits, largest finite value 448)
+ * with one fp32 scale per token for its K vector and one for its V vector.
+ * See pa_reshape_and_cache_fp8 and pa_decode_fp8. */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /* host-detected errors (negative return values) */
 #define PA_OK             0
@@ -130,6 +136,61 @@ int pa_decode(void* out, const void* query,
               pa_dtype dtype, void* stream);
 
 /*
+ * KV append into an e4m3 pool.  The write of pa_reshape_and_cache, with each
+ * token's K vector and V vector ([num_kv_heads, head_dim], every head)
+ * quantised on its own ([KVS] §19.2.4: per-token scaled quantisation, FP8
+ * at one byte per element).  The formula is not in the extracted page; the
+ * reading implemented is absmax scaling onto the e4m3 range:
+ *
+ *   amax  = max |x| over the token's vector
+ *   scale = amax / 448                 (fp32, correctly rounded)
+ *   code  = e4m3(x * (448 / amax))     (fp32 product, nearest-even rounding,
+ *                                       saturating at +-448)
+ *
+ * and amax == 0 gives scale 0 and all-zero codes.  A dequantised element is
+ * e4m3_value(code) * scale.  Non-finite inputs give unspecified codes.
+ *
+ *   key, value        [num_tokens, num_kv_heads, head_dim], src_dtype
+ *                     PA_BF16 or PA_F32
+ *   slot_mapping      as for pa_reshape_and_cache
+ *   k_cache, v_cache  e4m3 pools [num_blocks, block_size, num_kv_heads,
+ *                     head_dim], one byte per element
+ *   k_scale, v_scale  [num_blocks, block_size] fp32 (16-byte aligned): the
+ *                     scale of the token in each slot
+ */
+int pa_reshape_and_cache_fp8(const void* key, const void* value,
+                             const int64_t* slot_mapping, int num_tokens,
+                             void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                             int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                             pa_dtype src_dtype, void* stream);
+
+/*
+ * Paged decode attention over an e4m3 pool: the result of pa_decode over
+ * the dequantised pool (K = e4m3_value(code) * k_scale[slot], likewise V).
+ * The per-token scales are applied exactly in fp32: the K scale multiplies
+ * the token's score, the V scale its softmax weight in the P*V sum (the
+ * softmax normaliser uses the unscaled weights).  Halves the bytes read per
+ * token against bf16 ([KVS] §19.2.4).
+ *
+ *   query, out        dtype must be PA_BF16
+ *   k_cache, v_cache  e4m3 pools; k_scale, v_scale as written by
+ *                     pa_reshape_and_cache_fp8 (16-byte aligned)
+ *   other arguments   as for pa_decode; the workspace size is the same
+ *
+ * Runs on CUDA cores for every group size (fp32 products of the exactly
+ * widened codes).
+ */
+int pa_decode_fp8(void* out, const void* query,
+                  const void* k_cache, const void* v_cache,
+                  const float* k_scale, const float* v_scale,
+                  const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int num_seqs,
+                  int num_heads, int num_kv_heads, int head_dim,
+                  int block_size, int num_blocks, float scale, int partition_size,
+                  void* workspace, size_t workspace_bytes,
+                  pa_dtype dtype, void* stream);
+
+/*
  * Swap blocks between two pools (preemption by swapping).  [KVS] §19.2.6:
  * a preempted request's KV cache can be moved out to CPU memory and moved
  * back when GPU memory frees up; [OS] §九 names the same swap-out.  For each
@@ -146,7 +207,8 @@ int pa_decode(void* out, const void* query,
  *                 destination blocks distinct, pools not overlapping
  *
  * A pair naming a block outside its pool is skipped and sets
- * PA_DEV_BAD_BLOCK.  num_pairs == 0 launches nothing.
+ * PA_DEV_BAD_BLOCK.  num_pairs == 0 launches nothing.  Shapes and dtypes as
+ * for pa_copy_blocks (an e4m3 pool swaps its scale rows by a second call).
  */
 int pa_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks,
                    const void* src_k, const void* src_v, int src_num_blocks,
@@ -207,6 +269,12 @@ int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int 
  *
  * A pair with an id outside [0, num_blocks) is skipped and sets
  * PA_DEV_BAD_BLOCK.  num_pairs == 0 launches nothing.
+ *
+ * Pure byte movement, so any dtype (PA_FP8_E4M3 included) and any
+ * num_kv_heads, head_dim >= 1 whose block (block_size * num_kv_heads *
+ * head_dim * element bytes) is a multiple of 16 bytes.  For an e4m3 pool,
+ * copy its scale rows with a second call with the same pairs on
+ * (k_scale, v_scale) as an fp32 pool with num_kv_heads = head_dim = 1.
  */
 int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
                    int num_blocks, int block_size, int num_kv_heads, int head_dim,

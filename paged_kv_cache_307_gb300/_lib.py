@@ -21,7 +21,7 @@ if not os.path.exists(LIB_PATH):
 
 lib = ctypes.CDLL(LIB_PATH)
 
-PA_F32, PA_BF16 = 0, 1
+PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
 
 _p, _i, _f, _sz, _i64p, _i32p = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
@@ -41,6 +41,11 @@ lib.pa_copy_blocks.argtypes = [_p, _p, _i64p, _i, _i, _i, _i, _i, _i, _p]
 lib.pa_copy_blocks.restype = _i
 lib.pa_prefill_paged.argtypes = [_p, _p, _i, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
 lib.pa_prefill_paged.restype = _i
+lib.pa_reshape_and_cache_fp8.argtypes = [_p, _p, _i64p, _i, _p, _p, _p, _p, _i, _i, _i, _i, _i, _p]
+lib.pa_reshape_and_cache_fp8.restype = _i
+lib.pa_decode_fp8.argtypes = [_p, _p, _p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz,
+                              _i, _p]
+lib.pa_decode_fp8.restype = _i
 lib.pa_swap_blocks.argtypes = [_p, _p, _i, _p, _p, _i, _i64p, _i, _i, _i, _i, _i, _p]
 lib.pa_swap_blocks.restype = _i
 lib.pa_last_error.argtypes = []
@@ -73,6 +78,8 @@ def _dtype(t):
         return PA_F32
     if t.dtype == torch.bfloat16:
         return PA_BF16
+    if t.dtype == torch.uint8:
+        return PA_FP8_E4M3          # e4m3 codes
     raise TypeError("unsupported dtype %s" % t.dtype)
 
 
@@ -106,6 +113,19 @@ def reshape_and_cache(key, value, slot_mapping, k_cache, v_cache, stream=None):
                                     _stream(stream)), "pa_reshape_and_cache")
 
 
+def reshape_and_cache_fp8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """Quantise key/value [T, Hkv, D] (bf16 or fp32) per token into an e4m3
+    pool (uint8 codes [NB, bs, Hkv, D]) and its scales (fp32 [NB, bs])."""
+    _contig(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+    assert k_cache.dtype == torch.uint8 and k_scale.dtype == torch.float32
+    assert slot_mapping.dtype == torch.int64
+    NB, bs, H, D = k_cache.shape
+    assert k_scale.shape == (NB, bs) and v_scale.shape == (NB, bs)
+    _check(lib.pa_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
+                                        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), NB, bs, H, D,
+                                        _dtype(key), _stream(stream)), "pa_reshape_and_cache_fp8")
+
+
 def workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, partition_size=0):
     return lib.pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
                                          block_size, partition_size)
@@ -136,6 +156,30 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, partitio
                          ctypes.c_float(scale), partition_size, _ptr(workspace), workspace.numel(),
                          _dtype(q), _stream(stream)), "pa_decode")
     return out
+
+
+def decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+               partition_size=0, workspace=None, stream=None):
+    """out[B,Hq,D] (bf16) = paged decode attention of q over an e4m3 pool."""
+    _contig(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert k_cache.dtype == torch.uint8 and k_scale.dtype == torch.float32
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if workspace is None:
+        workspace = alloc_workspace(q, k_cache, block_tables, partition_size)
+    _check(lib.pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
+                             ctypes.c_float(scale), partition_size, _ptr(workspace), workspace.numel(), _dtype(q),
+                             _stream(stream)), "pa_decode_fp8")
+    return out
+
+
+def copy_blocks_fp8(k_cache, v_cache, k_scale, v_scale, pairs, stream=None):
+    """Copy-on-write for an e4m3 pool: the codes, then the scale rows."""
+    copy_blocks(k_cache, v_cache, pairs, stream)
+    NB, bs = k_scale.shape
+    copy_blocks(k_scale.view(NB, bs, 1, 1), v_scale.view(NB, bs, 1, 1), pairs, stream)
 
 
 def copy_blocks(k_cache, v_cache, pairs, stream=None):

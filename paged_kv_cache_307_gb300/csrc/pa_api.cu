@@ -64,26 +64,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-bool encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int num_blocks, int block_size,
-                     int num_kv_heads, int head_dim) {
-  auto fn = get_encode_fn();
-  if (!fn) return false;
-  const cuuint64_t e = (cuuint64_t)elem_bytes(dt);
-  // innermost first: head_dim, kv head, slot in block, block
-  cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
-                        (cuuint64_t)num_blocks};
-  cuuint64_t strides[3] = {head_dim * e, (cuuint64_t)num_kv_heads * head_dim * e,
-                           (cuuint64_t)block_size * num_kv_heads * head_dim * e};
-  cuuint32_t box[4] = {(cuuint32_t)head_dim, 1, (cuuint32_t)block_size, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, dt == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-bool encode_map(CUtensorMap* map, const void* base, bool f32, int rank, const uint64_t* dims,
+bool encode_map(CUtensorMap* map, const void* base, pa_dtype dt, int rank, const uint64_t* dims,
                 const uint64_t* strides, const uint32_t* box, bool swizzle128) {
   auto fn = get_encode_fn();
   if (!fn) return false;
@@ -95,7 +76,10 @@ bool encode_map(CUtensorMap* map, const void* base, bool f32, int rank, const ui
     e[i] = 1;
     if (i + 1 < rank) st[i] = strides[i];
   }
-  CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+  const CUtensorMapDataType ty = dt == PA_F32         ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dt == PA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, ty, rank,
                   const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -107,7 +91,7 @@ bool encode_map(CUtensorMap* map, const void* base, bool f32, int rank, const ui
 extern "C" int pa_last_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   const unsigned a = pa::fetch_status_cache_ops();
-  const unsigned b = pa::fetch_status_decode();
+  const unsigned b = pa::fetch_status_decode() | pa::fetch_status_decode_fp8();
   const unsigned c = pa::fetch_status_prefill();
   if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) return PA_ERR_CUDA;
   return (int)(a | b | c);

@@ -9,6 +9,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda.h>
 #include <stdint.h>
 
@@ -84,6 +85,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Untiled bulk copy global -> shared completing on an mbarrier; both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -150,7 +161,31 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
 
-inline int elem_bytes(pa_dtype dt) { return dt == PA_F32 ? 4 : 2; }
+// Tag type for e4m3 codes in a K/V pool (one byte per element).
+struct fp8e4m3 {
+  uint8_t bits;
+};
+// Two e4m3 codes (low byte = first element) to two floats, exactly.
+__device__ __forceinline__ void e4m3x2_to_float2(uint32_t two, float& lo, float& hi) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  lo = f.x;
+  hi = f.y;
+}
+template <> struct Elem<fp8e4m3> {
+  static constexpr int kBytes = 1;
+  static constexpr int kPerChunk = 16;
+  __device__ __forceinline__ static void unpack(const uint4& c, float* f) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e4m3x2_to_float2(w[i], f[4 * i], f[4 * i + 1]);
+      e4m3x2_to_float2(w[i] >> 16, f[4 * i + 2], f[4 * i + 3]);
+    }
+  }
+};
+
+inline int elem_bytes(pa_dtype dt) { return dt == PA_F32 ? 4 : dt == PA_FP8_E4M3 ? 1 : 2; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -160,15 +195,11 @@ inline bool supported_block_size(int bs) { return bs == 4 || bs == 8 || bs == 16
 // Host: number of SMs on the current device (cached per device).
 int device_sm_count();
 
-// Host: encode a 4-D tiled tensor map for a [NB, bs, H, D] pool with a box
-// of {D, 1, bs, 1} (one head of one block).  Returns false on failure.
-bool encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int num_blocks,
-                     int block_size, int num_kv_heads, int head_dim);
 
 // Host: encode a tiled tensor map of rank <= 5 (dims/box innermost first,
 // strides in bytes for dims 1..rank-1), bf16 or fp32, optionally with the
 // 128-byte shared-memory swizzle.  Returns false on failure.
-bool encode_map(CUtensorMap* map, const void* base, bool f32, int rank, const uint64_t* dims,
+bool encode_map(CUtensorMap* map, const void* base, pa_dtype dt, int rank, const uint64_t* dims,
                 const uint64_t* strides, const uint32_t* box, bool swizzle128);
 
 // Host: record the text of the last host-side failure (per thread); read
@@ -183,6 +214,7 @@ bool raise_smem_limit(const void* kernel, int dev);
 // Per-translation-unit status fetch (returns the sticky word and clears it).
 unsigned fetch_status_cache_ops();
 unsigned fetch_status_decode();
+unsigned fetch_status_decode_fp8();
 unsigned fetch_status_prefill();
 
 }  // namespace pa

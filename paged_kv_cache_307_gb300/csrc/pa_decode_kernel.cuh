@@ -1,0 +1,696 @@
+// pa_decode_kernel.cuh — the paged decode attention kernel and its merge kernel,
+// shared by the translation units that instantiate them (pa_decode.cu: f32 and
+// bf16 pools; pa_decode_fp8.cu: e4m3 pools).  Each including unit gets its own
+// copy of the kernels and its own sticky status word (internal linkage).
+//
+// What it computes ("19.2 KV Cache 系统化管理" §19.2.3 and Fig 19-5; "LLM 推理
+// 引擎的内存管理与调度…" §三): for each sequence b and query head h, attention of
+// q[b,h] over the sequence's K/V, which sit in fixed-size physical blocks named
+// by the block table; only the valid slots of the last block count; the
+// softmax is accumulated block by block with a running maximum, a running sum
+// of exponentials and a rescaled output, normalised at the end.
+//
+// How (GB300):
+//  * Work item = (sequence, KV head, query-head subgroup, partition of P
+//    tokens).  A persistent grid (resident CTAs x SMs) strides over the item
+//    space; the sequence index is innermost so CTAs running side by side read
+//    the same blocks when sequences share a prompt.
+//  * Each CTA = 1 producer warp + kConsumerWarps consumer warps.  The producer
+//    reads the item's block-table entries with one coalesced warp load, then
+//    issues, per block, two TMA tensor loads (box {D, 1 head, bs, 1 block} of
+//    the [NB, bs, Hkv, D] pool) for K and V into a ring of shared-memory
+//    stages, completing on an mbarrier with transaction bytes.  A block id
+//    outside the pool is flagged and replaced by block 0, so no copy leaves
+//    the pool.
+//  * Consumer warps take the item's blocks round-robin, and each warp owns its
+//    own ring of SPW stages which it consumes strictly in order (a ring shared
+//    by several round-robin consumers lets a warp wait on a stage two phases
+//    ahead, where a parity wait matches the stale phase).  Inside a warp, LPT
+//    lanes share one token (each lane owns two 16-byte chunks of head_dim), so
+//    one warp covers TPW tokens per pass with conflict-free 16-byte shared
+//    loads.  Each lane group keeps its own online-softmax state (m, l, o) for
+//    its tokens; group, warp and partition states are merged by log-sum-exp at
+//    the end, which is exact up to rounding (the update is associative).
+//  * Scores are computed in the base-2 domain (q pre-multiplied by
+//    scale*log2 e), with exp2f.  The K/V rows are read once from HBM and used
+//    for all GT query heads of the subgroup (GQA) straight from registers.
+//  * A sequence whose context fits one partition is normalised and written
+//    directly; longer ones write (m, l, unnormalised o) per partition to the
+//    workspace, and merge_kernel combines them.
+//  * Waits are bounded (2 s).  A wait that runs out sets PA_DEV_TIMEOUT and an
+//    abort flag; every role then skips the remaining work while still passing
+//    the CTA's barriers, and the producer waits (bounded) for the TMA loads it
+//    issued before the CTA exits.
+#pragma once
+
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_status_decode;
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kSmemAlign = 1024;
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_ml;       // [B*Hq*max_parts][2]   (m in log2 units, l)
+  float* ws_o;        // [B*Hq*max_parts][D]   unnormalised output
+  int B, Hq, Hkv, G, nsub;
+  int max_blocks, bs, num_blocks;
+  int part_tokens, max_parts;
+  long long n_virtual;
+  float qscale;       // scale * log2(e)
+  const float* k_scale;  // e4m3 pools: per-token K scales [num_blocks * bs]; else null
+  const float* v_scale;  // e4m3 pools: per-token V scales
+  int HG;             // KV heads per work item (one consumer warp each when HG = 4)
+  int n_hg;           // Hkv / HG
+  int WPH;            // warp groups: kConsumerWarps / HG (warps sharing one head)
+  int spg;            // shared-memory stages per warp group
+  uint32_t tile_bytes;  // one head's K (or V) tile of one block: bs * D * elem
+};
+
+struct Item {
+  int b, kvh0, sg, part, t1, jb, je;
+  bool split;
+};
+
+// m16n8k16 bf16 tensor-core product with fp32 accumulation (per warp).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, Item& it) {
+  it.b = (int)(v % p.B);
+  long long r = v / p.B;
+  it.kvh0 = (int)(r % p.n_hg) * p.HG;
+  r /= p.n_hg;
+  it.sg = (int)(r % p.nsub);
+  it.part = (int)(r / p.nsub);
+  int L = __ldg(&p.context_lens[it.b]);
+  const int Lmax = p.max_blocks * p.bs;
+  if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;   // flagged by the consumer
+  const int nparts = L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+  if (it.part >= nparts) return false;
+  const int t0 = it.part * p.part_tokens;
+  it.t1 = min(L, t0 + p.part_tokens);
+  it.jb = t0 / p.bs;
+  it.je = (it.t1 + p.bs - 1) / p.bs;
+  if (it.je < it.jb) it.je = it.jb;
+  it.split = nparts > 1;
+  return true;
+}
+
+// T: query/output element type; KT: K/V pool element type (T itself, or
+// e4m3 codes with a per-token scale for K and for V).
+template <typename T, typename KT, int D, int GT, bool MMA, int HG>
+__global__ void __launch_bounds__(kThreads)
+decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+              const DecodeParams p) {
+  using E = Elem<T>;                           // queries and output
+  using EK = Elem<KT>;                         // K/V pool
+  constexpr bool SCALED = EK::kBytes == 1;     // e4m3 codes with per-token scales
+  constexpr int CHUNKS = D * EK::kBytes / 16;  // 16-byte chunks per token row
+  // chunks per lane: two, except for e4m3 with several query heads, where
+  // two chunks (32 dims) per lane would need 2*GT*32 registers for q and o
+  constexpr int CPL = (SCALED && GT > 1) ? 1 : 2;
+  constexpr int LPT = CHUNKS / CPL;            // lanes per token
+  constexpr int TPW = 32 / LPT;                // tokens per warp pass
+  constexpr int EPC = EK::kPerChunk;           // elements per chunk
+  constexpr int DPL = CPL * EPC;               // head dims per lane
+  constexpr int NS = TPW >= 16 ? 1 : 16 / TPW; // tokens per lane group per softmax step
+  constexpr int ROW = D * EK::kBytes;          // one head's K (or V) row
+  constexpr int QROW = D * E::kBytes;          // one head's query (or output) row
+  constexpr int QPC = EPC / E::kPerChunk;      // query 16-byte loads per K/V chunk
+  constexpr int NCW = kConsumerWarps;
+  static_assert(LPT >= 1 && LPT <= 32 && (32 % LPT) == 0, "lane split");
+  static_assert(QPC >= 1 && EPC % E::kPerChunk == 0, "query chunking");
+  static_assert(!(SCALED && MMA), "e4m3 pools use the CUDA-core path");
+
+  constexpr int WPH = kConsumerWarps / HG;               // warp groups (warps sharing a head)
+  static_assert(HG == 1 || HG == 2 || HG == 4, "KV heads per item");
+  const int S = p.spg * WPH;                             // stages in total
+  const uint32_t stage_bytes = (uint32_t)HG * p.tile_bytes;  // K (or V) of one block, HG heads
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // TMA destinations must be 128-byte aligned: align the base explicitly
+  // (the host reserves kSmemAlign bytes of slack).
+  unsigned char* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
+  unsigned char* tilesK = smem;
+  unsigned char* tilesV = smem + (size_t)S * stage_bytes;
+  // e4m3 pools: each stage also holds the block's bs K scales and bs V scales
+  float* sclK = reinterpret_cast<float*>(tilesV + (size_t)S * stage_bytes);
+  float* sclV = sclK + (SCALED ? S * p.bs : 0);
+  float* mbuf = sclV + (SCALED ? S * p.bs : 0);
+  uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + NCW * GT * (D + 2));
+  uint64_t* empty = full + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], HG);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // An item covers HG KV heads.  Consumer warp w works on head w % HG of
+  // the item, in warp group w / HG; block i of the item goes to group
+  // i % WPH (WPH = NCW / HG), and every warp of that group reads its own head
+  // from the same stage.  Each group owns SPW stages which all its warps
+  // consume strictly in order, so every stage has one producer and one set of
+  // consumers that walk its phases in order and a parity wait can never match
+  // a stale phase.  u = the group's running block count (same arithmetic in
+  // every role); stage = g*SPW + u % SPW.  The HG heads of a block are loaded
+  // back to back, so the DRAM sees neighbouring rows of the pool together.
+  const int SPW = p.spg;
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&mapK);
+      prefetch_tensormap(&mapV);
+    }
+    const uint64_t pol = policy_evict_first();
+    // base[g] = warp group g's running block count, issued[g] = loads issued
+    // into its stages (WPH is a compile-time constant, so the group
+    // arithmetic below is shifts and selects).
+    uint32_t base[NCW], issued[NCW];
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) base[w] = issued[w] = 0;
+    for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
+      Item item;
+      if (!decode_item(p, v, item)) continue;
+      const int32_t* row = p.block_tables + (size_t)item.b * p.max_blocks;
+      const int nblk = item.je - item.jb;
+      for (int j0 = 0; j0 < nblk; j0 += 32) {
+        const int n = min(32, nblk - j0);
+        int blk = 0;
+        if (lane < n) {
+          blk = __ldg(&row[item.jb + j0 + lane]);
+          if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            atomicOr(&g_status_decode, PA_DEV_BAD_BLOCK);
+            blk = 0;    // keep every copy inside the pool
+          }
+        }
+        for (int i = 0; i < n; ++i) {
+          const int bi = __shfl_sync(0xffffffffu, blk, i);
+          const int w = (j0 + i) % WPH;
+          uint32_t u = 0;
+#pragma unroll
+          for (int k = 0; k < WPH; ++k)
+            if (k == w) u = base[k] + (uint32_t)((j0 + i) / WPH);
+          const int st = w * SPW + (int)(u % SPW);
+          const uint32_t ph = (u / SPW) & 1u;
+          constexpr int HALVES = MMA ? D / 64 : 1;
+          constexpr int NOPS = MMA ? 2 * HG * HALVES : 2;   // TMA loads per block
+          int go = 0;
+          if (lane == 0 && !*abort_flag) {
+            if (!mbar_wait(&empty[st], ph ^ 1u)) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            } else {
+              mbar_arrive_expect_tx(&full[st], 2u * stage_bytes + (SCALED ? 8u * (uint32_t)p.bs : 0u));
+              go = 1;
+              if constexpr (NOPS == 2) {
+                // one box {D, HG heads, bs, 1} each for K and V: smem [bs][HG][D]
+                tma_load_4d(tilesK + (size_t)st * stage_bytes, &mapK, &full[st], 0, item.kvh0, 0, bi, pol);
+                tma_load_4d(tilesV + (size_t)st * stage_bytes, &mapV, &full[st], 0, item.kvh0, 0, bi, pol);
+              }
+              if constexpr (SCALED) {
+                // the block's scale rows: bs fp32 values each, contiguous
+                bulk_load(sclK + st * p.bs, p.k_scale + (size_t)bi * p.bs, 4u * p.bs, &full[st], pol);
+                bulk_load(sclV + st * p.bs, p.v_scale + (size_t)bi * p.bs, 4u * p.bs, &full[st], pol);
+              }
+            }
+          }
+          if constexpr (NOPS > 2) {
+            // tensor-core path: many 128-byte-swizzled 64-column halves per
+            // block, issued by one warp instruction: lane l takes K (l even)
+            // or V (l odd) of head l/2/HALVES, half l/2%HALVES
+            if (__shfl_sync(0xffffffffu, go, 0) && lane < NOPS) {
+              const int rest = lane >> 1;
+              const int hl = rest / HALVES, hh = rest % HALVES;
+              const size_t off = (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes + (size_t)hh * p.bs * 128;
+              unsigned char* dst = ((lane & 1) ? tilesV : tilesK) + off;
+              tma_load_4d(dst, (lane & 1) ? &mapV : &mapK, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
+            }
+          }
+          if (lane == 0 && go) {
+#pragma unroll
+            for (int k = 0; k < WPH; ++k)
+              if (k == w) issued[k] = u + 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < WPH; ++w) base[w] += nblk > w ? (uint32_t)((nblk - w + WPH - 1) / WPH) : 0u;
+    }
+    // Never leave the CTA with TMA writes into its shared memory in flight:
+    // wait (bounded) for the last SPW loads issued into each group's stages.
+    if (lane == 0) {
+#pragma unroll
+      for (int w = 0; w < WPH; ++w) {
+        const uint32_t first = issued[w] > (uint32_t)SPW ? issued[w] - SPW : 0u;
+        for (uint32_t u = first; u < issued[w]; ++u)
+          mbar_wait(&full[w * SPW + (int)(u % SPW)], (u / SPW) & 1u);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int grp = lane / LPT;     // token slot within a warp pass
+  const int li = lane % LPT;      // chunk owner within the token row
+  // this lane owns chunks li + j*LPT of each row, j < CPL
+  const int ctid = threadIdx.x;   // 0 .. NCW*32-1
+  uint32_t wcount = 0;            // blocks this warp's group has consumed so far
+  const int hl = warp % HG;       // the item's KV head this warp works on
+  const int gw = warp / HG;       // this warp's group
+
+  for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
+    Item item;
+    if (!decode_item(p, v, item)) continue;
+    if (ctid == 0 && item.kvh0 == 0 && item.sg == 0 && item.part == 0) {
+      const int L = __ldg(&p.context_lens[item.b]);
+      if (L < 0 || L > p.max_blocks * p.bs) atomicOr(&g_status_decode, PA_DEV_BAD_LEN);
+    }
+    const int h0 = (item.kvh0 + hl) * p.G + item.sg * GT;
+
+    if constexpr (MMA) {
+      // Query heads h0..h0+GT-1 are the M rows of m16n8k16 (rows >= GT are
+      // zero); K rows are the N columns of S = Q K^T, and P (bf16) times V
+      // accumulates O[16 x D] in registers.  Lane (g = lane/4, tq = lane%4)
+      // holds rows g and g+8.  K/V tiles sit in shared memory as 128-byte-
+      // swizzled 64-column halves, so ldmatrix reads are conflict-free.
+      constexpr int KS = D / 16;
+      constexpr int NT = D / 8;
+      const int g = lane >> 2, tq = lane & 3;
+      const bool r0v = g < GT, r1v = g + 8 < GT;
+      const uint32_t* q0p = reinterpret_cast<const uint32_t*>(
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + (r0v ? g : 0)) * QROW);
+      const uint32_t* q1p = reinterpret_cast<const uint32_t*>(
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + (r1v ? g + 8 : 0)) * QROW);
+      uint32_t qa[KS][4];
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qa[kk][0] = r0v ? __ldg(q0p + kk * 8 + tq) : 0u;
+        qa[kk][1] = r1v ? __ldg(q1p + kk * 8 + tq) : 0u;
+        qa[kk][2] = r0v ? __ldg(q0p + kk * 8 + 4 + tq) : 0u;
+        qa[kk][3] = r1v ? __ldg(q1p + kk * 8 + 4 + tq) : 0u;
+      }
+      float O[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
+      float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};
+      const uint32_t half_bytes = (uint32_t)p.bs * 128u;
+
+      const int nblk = item.je - item.jb;
+      for (int i = gw; i < nblk; i += WPH, ++wcount) {
+        const int st = gw * SPW + (int)(wcount % SPW);
+        const uint32_t ph = (wcount / SPW) & 1u;
+        bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        if (live) {
+          const bool late = !mbar_wait(&full[st], ph);
+          if (__any_sync(0xffffffffu, late)) {
+            live = false;
+            if (lane == 0) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          }
+        }
+        if (live) {
+          const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
+          unsigned char* vt_ptr = tilesV + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
+          const uint32_t kt = smem_u32(tilesK + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes);
+          const uint32_t vt = smem_u32(vt_ptr);
+          if (valid < p.bs) {
+            // slots past the context may hold anything; P is 0 there, but
+            // 0 * NaN is NaN inside the product, so clear those V rows
+            for (int idx = lane; idx < (p.bs - valid) * (D / 8); idx += 32) {
+              const int t = valid + idx / (D / 8), c = idx % (D / 8);
+              *reinterpret_cast<uint4*>(vt_ptr + (c >> 3) * half_bytes + t * 128 + (c & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          for (int tb = 0; tb < valid; tb += 16) {
+            float S[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+              const int tt = min(tb + (lane & 7) + ((lane >> 4) << 3), p.bs - 1);
+#pragma unroll
+              for (int kk = 0; kk < KS; ++kk) {
+                const int c = 2 * kk + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), b0, b1, b2, b3);
+                mma_bf16_16816(S[0], qa[kk], b0, b1);
+                mma_bf16_16816(S[1], qa[kk], b2, b3);
+              }
+            }
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int t = tb + n * 8 + 2 * tq + (e & 1);
+                S[n][e] = t < valid ? S[n][e] * p.qscale : -INFINITY;
+                mx[e >> 1] = fmaxf(mx[e >> 1], S[n][e]);
+              }
+            float alpha[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+              mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+              const float mn = fmaxf(mr[r], mx[r]);
+              alpha[r] = mn == -INFINITY ? 1.f : exp2f(mr[r] - mn);
+              mr[r] = mn;
+              lr[r] *= alpha[r];
+            }
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+              for (int n = 0; n < NT; ++n) {
+                O[n][0] *= alpha[0];
+                O[n][1] *= alpha[0];
+                O[n][2] *= alpha[1];
+                O[n][3] *= alpha[1];
+              }
+            }
+            float pv[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float m_ = mr[e >> 1];
+                pv[n][e] = (S[n][e] == -INFINITY) ? 0.f : exp2f(S[n][e] - m_);
+                lr[e >> 1] += pv[n][e];
+              }
+            const uint32_t pa[4] = {pack_bf16(pv[0][0], pv[0][1]), pack_bf16(pv[0][2], pv[0][3]),
+                                    pack_bf16(pv[1][0], pv[1][1]), pack_bf16(pv[1][2], pv[1][3])};
+            {
+              const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
+#pragma unroll
+              for (int j = 0; j < D / 16; ++j) {
+                const int c = 2 * j + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), b0, b1, b2, b3);
+                mma_bf16_16816(O[2 * j], pa, b0, b1);
+                mma_bf16_16816(O[2 * j + 1], pa, b2, b3);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      // the row sums are split over the 4 lanes of a row group
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 1);
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int h = g + 8 * r;
+        if (h < GT) {
+          float* dst = mbuf + (warp * GT + h) * (D + 2);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            dst[n * 8 + 2 * tq] = O[n][2 * r];
+            dst[n * 8 + 2 * tq + 1] = O[n][2 * r + 1];
+          }
+          if (tq == 0) {
+            dst[D] = mr[r];
+            dst[D + 1] = lr[r];
+          }
+        }
+      }
+    } else {
+      float q[GT][DPL];
+  #pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        const unsigned char* qrow =
+            static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + h) * QROW;
+        // this lane's head dims: its CPL K/V chunks, EPC dims each
+  #pragma unroll
+        for (int hf = 0; hf < CPL; ++hf) {
+  #pragma unroll
+          for (int j = 0; j < QPC; ++j) {
+            float f[E::kPerChunk];
+            const int d0 = (li + hf * LPT) * EPC + j * E::kPerChunk;
+            E::unpack(__ldg(reinterpret_cast<const uint4*>(qrow + (size_t)d0 * E::kBytes)), f);
+  #pragma unroll
+            for (int e = 0; e < E::kPerChunk; ++e) q[h][hf * EPC + j * E::kPerChunk + e] = f[e] * p.qscale;
+          }
+        }
+      }
+      float m[GT], l[GT], o[GT][DPL];
+  #pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+  #pragma unroll
+        for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
+      }
+
+      const int nblk = item.je - item.jb;
+      for (int i = gw; i < nblk; i += WPH, ++wcount) {
+        const int st = gw * SPW + (int)(wcount % SPW);
+        const uint32_t ph = (wcount / SPW) & 1u;
+        bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        if (live) {
+          const bool late = !mbar_wait(&full[st], ph);
+          if (__any_sync(0xffffffffu, late)) {
+            live = false;
+            if (lane == 0) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          }
+        }
+        if (live) {
+          const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
+          // stage layout [bs][HG][D]: token t of head hl at (t*HG + hl) * ROW
+          const unsigned char* kt = tilesK + (size_t)st * stage_bytes + (size_t)hl * ROW;
+          const unsigned char* vt = tilesV + (size_t)st * stage_bytes + (size_t)hl * ROW;
+          for (int tb = 0; tb < valid; tb += TPW * NS) {
+            float s[NS][GT];
+  #pragma unroll
+            for (int k = 0; k < NS; ++k) {
+              const int t = tb + k * TPW + grp;
+              const bool ok = t < valid;
+              float part[GT];
+  #pragma unroll
+              for (int h = 0; h < GT; ++h) part[h] = 0.f;
+              if (ok) {
+                float kf[DPL];
+  #pragma unroll
+                for (int hf = 0; hf < CPL; ++hf)
+                  EK::unpack(*reinterpret_cast<const uint4*>(kt + t * (HG * ROW) + (li + hf * LPT) * 16),
+                             kf + hf * EPC);
+  #pragma unroll
+                for (int h = 0; h < GT; ++h)
+  #pragma unroll
+                  for (int d = 0; d < DPL; ++d) part[h] = fmaf(q[h][d], kf[d], part[h]);
+              }
+              // e4m3: the token's K scale multiplies its whole score
+              float ksc = 1.f;
+              if constexpr (SCALED) ksc = ok ? sclK[st * p.bs + t] : 0.f;
+  #pragma unroll
+              for (int h = 0; h < GT; ++h) {
+  #pragma unroll
+                for (int off = LPT / 2; off > 0; off >>= 1)
+                  part[h] += __shfl_xor_sync(0xffffffffu, part[h], off);
+                s[k][h] = ok ? part[h] * ksc : -INFINITY;
+              }
+            }
+  #pragma unroll
+            for (int h = 0; h < GT; ++h) {
+              float mx = m[h];
+  #pragma unroll
+              for (int k = 0; k < NS; ++k) mx = fmaxf(mx, s[k][h]);
+              const float alpha = mx == -INFINITY ? 1.f : exp2f(m[h] - mx);
+              m[h] = mx;
+              l[h] *= alpha;
+  #pragma unroll
+              for (int d = 0; d < DPL; ++d) o[h][d] *= alpha;
+            }
+  #pragma unroll
+            for (int k = 0; k < NS; ++k) {
+              const int t = tb + k * TPW + grp;
+              if (t < valid) {
+                float vf[DPL];
+  #pragma unroll
+                for (int hf = 0; hf < CPL; ++hf)
+                  EK::unpack(*reinterpret_cast<const uint4*>(vt + t * (HG * ROW) + (li + hf * LPT) * 16),
+                             vf + hf * EPC);
+                // e4m3: the token's V scale rides on its softmax weight
+                float vsc = 1.f;
+                if constexpr (SCALED) vsc = sclV[st * p.bs + t];
+  #pragma unroll
+                for (int h = 0; h < GT; ++h) {
+                  const float pk = exp2f(s[k][h] - m[h]);
+                  l[h] += pk;
+                  const float pw = SCALED ? pk * vsc : pk;
+  #pragma unroll
+                  for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(pw, vf[d], o[h][d]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+
+      // merge the lane groups of this warp (lanes with equal li own equal dims)
+  #pragma unroll
+      for (int off = LPT; off < 32; off <<= 1) {
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m[h], off);
+          const float l2 = __shfl_xor_sync(0xffffffffu, l[h], off);
+          const float M = fmaxf(m[h], m2);
+          const float a = m[h] == -INFINITY ? 0.f : exp2f(m[h] - M);
+          const float b = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
+          l[h] = a * l[h] + b * l2;
+  #pragma unroll
+          for (int d = 0; d < DPL; ++d) {
+            const float o2 = __shfl_xor_sync(0xffffffffu, o[h][d], off);
+            o[h][d] = a * o[h][d] + b * o2;
+          }
+          m[h] = M;
+        }
+      }
+      if (grp == 0) {
+  #pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          float* dst = mbuf + (warp * GT + h) * (D + 2);
+  #pragma unroll
+          for (int e = 0; e < EPC; ++e) {
+  #pragma unroll
+            for (int hf = 0; hf < CPL; ++hf) dst[(li + hf * LPT) * EPC + e] = o[h][hf * EPC + e];
+          }
+          if (li == 0) {
+            dst[D] = m[h];
+            dst[D + 1] = l[h];
+          }
+        }
+      }
+    }
+    named_sync(1, NCW * 32);
+
+    // merge the warp groups (warps gw*HG + hl share head hl) and write
+    for (int idx = ctid; idx < HG * GT * D; idx += NCW * 32) {
+      const int hh = idx / (GT * D), h = (idx / D) % GT, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < WPH; ++g) M = fmaxf(M, mbuf[((g * HG + hh) * GT + h) * (D + 2) + D]);
+      float num = 0.f, den = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int g = 0; g < WPH; ++g) {
+          const float* src = mbuf + ((g * HG + hh) * GT + h) * (D + 2);
+          const float a = src[D] == -INFINITY ? 0.f : exp2f(src[D] - M);
+          num = fmaf(a, src[d], num);
+          den = fmaf(a, src[D + 1], den);
+        }
+      }
+      const size_t bh = (size_t)item.b * p.Hq + (size_t)(item.kvh0 + hh) * p.G + item.sg * GT + h;
+      if (!item.split) {
+        E::store1(static_cast<T*>(p.out) + bh * D + d, den > 0.f ? num / den : 0.f);
+      } else {
+        const size_t slot = bh * p.max_parts + item.part;
+        p.ws_o[slot * D + d] = num;
+        if (d == 0) {
+          p.ws_ml[slot * 2] = M;
+          p.ws_ml[slot * 2 + 1] = den;
+        }
+      }
+    }
+    named_sync(1, NCW * 32);
+  }
+}
+
+// One warp per (sequence, query head) with more than one partition.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+merge_kernel(const DecodeParams p) {
+  using E = Elem<T>;
+  constexpr int PER = D / 32;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)p.B * p.Hq) return;
+  const int b = (int)(gw / p.Hq);
+  int L = __ldg(&p.context_lens[b]);
+  const int Lmax = p.max_blocks * p.bs;
+  if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;
+  const int nparts = L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+  if (nparts <= 1) return;
+  const size_t base = (size_t)gw * p.max_parts;
+  float M = -INFINITY;
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[(base + i) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float den = 0.f;
+  for (int i = lane; i < nparts; i += 32) {
+    const float mi = p.ws_ml[(base + i) * 2];
+    if (mi != -INFINITY) den += exp2f(mi - M) * p.ws_ml[(base + i) * 2 + 1];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  for (int i = 0; i < nparts; ++i) {
+    const float mi = p.ws_ml[(base + i) * 2];
+    const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
+    const float* oi = p.ws_o + (base + i) * D;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oi[lane + 32 * k], acc[k]);
+  }
+  T* out = static_cast<T*>(p.out) + (size_t)gw * D;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) E::store1(out + lane + 32 * k, den > 0.f ? acc[k] / den : 0.f);
+}
+
+}  // namespace
+
+// A decode kernel and the merge kernel that goes with it.
+struct Launch {
+  const void* kernel;
+  const void* merge;
+};
+
+// e4m3-pool instances (pa_decode_fp8.cu): bf16 queries, CUDA-core path,
+// hg KV heads per work item.
+Launch pick_decode_fp8(int head_dim, int gt, int hg);
+
+}  // namespace pa

@@ -431,7 +431,7 @@ extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, c
     const uint64_t dims[4] = {128, (uint64_t)num_heads, (uint64_t)num_queries, (uint64_t)num_seqs};
     const uint64_t str[3] = {256, (uint64_t)num_heads * 256, (uint64_t)num_queries * num_heads * 256};
     const uint32_t box[4] = {64, (uint32_t)G, (uint32_t)QP, 1};
-    if (!encode_map(&mapQ, query, false, 4, dims, str, box, true)) {
+    if (!encode_map(&mapQ, query, PA_BF16, 4, dims, str, box, true)) {
       note_host_error("cuTensorMapEncodeTiled failed for the query tile");
       return PA_ERR_CUDA;
     }
@@ -440,8 +440,8 @@ extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, c
     const uint64_t dims[4] = {128, (uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
     const uint64_t str[3] = {256, (uint64_t)num_kv_heads * 256, (uint64_t)block_size * num_kv_heads * 256};
     const uint32_t box[4] = {64, 1, (uint32_t)block_size, 1};
-    if (!encode_map(&mapK, k_cache, false, 4, dims, str, box, true) ||
-        !encode_map(&mapV, v_cache, false, 4, dims, str, box, true)) {
+    if (!encode_map(&mapK, k_cache, PA_BF16, 4, dims, str, box, true) ||
+        !encode_map(&mapV, v_cache, PA_BF16, 4, dims, str, box, true)) {
       note_host_error("cuTensorMapEncodeTiled failed for the K/V pool");
       return PA_ERR_CUDA;
     }

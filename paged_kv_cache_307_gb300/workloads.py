@@ -347,13 +347,60 @@ def prefill_flops(lens, Tq, Hq, D):
     return 4 * tot * Hq * D
 
 
+def fp8_case(case, seed=None):
+    """The same workload over an e4m3 pool (uint8 codes) with per-token fp32
+    scales in ``extra['k_scale']``/``extra['v_scale']`` ([NB, bs]).
+
+    Input generation only: the codes are the pool's N(0,1) values times 112
+    (so about 4 standard deviations reach the top of the e4m3 range), clipped
+    to +-448 and cast by torch's float8_e4m3fn conversion, the way the other
+    cases round their draws to bf16; each slot's scales are drawn uniformly
+    from [0.5, 1.5] / 112.  Slots that hold NaN in the source pool get the
+    NaN code and a NaN scale.  q, key and value keep their dtype; the new
+    tokens are quantised by whoever appends them."""
+    seed = case.spec.seed if seed is None else seed
+    rng = np.random.default_rng(seed + 77)
+    NB, bs = case.k_cache.shape[:2]
+    dev = case.k_cache.device
+
+    def codes(pool):
+        out = torch.empty(pool.shape, dtype=torch.uint8, device=dev)
+        step = max(1, (1 << 26) // max(1, pool[0].numel()))
+        for i in range(0, NB, step):
+            x = pool[i:i + step].float() * 112.0
+            out[i:i + step] = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        return out
+
+    def scales(pool):
+        sc = torch.from_numpy(rng.uniform(0.5, 1.5, size=(NB, bs)).astype(np.float32) / np.float32(112)).to(dev)
+        nan = torch.isnan(pool.float()).flatten(2).any(-1) if NB * bs * pool[0, 0].numel() < (1 << 28) else \
+            torch.cat([torch.isnan(pool[i:i + 4096].float()).flatten(2).any(-1) for i in range(0, NB, 4096)])
+        sc[nan] = float("nan")
+        return sc
+
+    ks, vs = scales(case.k_cache), scales(case.v_cache)
+    kc, vc = codes(case.k_cache), codes(case.v_cache)
+    extra = dict(case.extra, k_scale=ks, v_scale=vs, kv="fp8")
+    return DecodeCase(case.spec, case.scale, case.q, kc, vc, case.block_tables, case.context_lens, case.key,
+                      case.value, case.slot_mapping, extra)
+
+
+def _kv_token_bytes(case):
+    """Pool bytes per token of context: K and V rows of every KV head, plus
+    the two fp32 scales of an e4m3 pool."""
+    s = case.spec
+    scl = 8 if case.extra.get("kv") == "fp8" else 0
+    return 2 * s.Hkv * s.D * case.k_cache.element_size() + scl
+
+
 def algorithmic_decode_bytes(case):
     """HBM bytes a decode call must move at least: K and V rows of every token
-    in context, Q in, O out, the block-table entries used, the lengths."""
+    in context (and their scales for an e4m3 pool), Q in, O out, the
+    block-table entries used, the lengths."""
     s = case.spec
     e = case.q.element_size()
     lens = case.context_lens.cpu().numpy().astype(np.int64)
-    kv = int(lens.sum()) * 2 * s.Hkv * s.D * e
+    kv = int(lens.sum()) * _kv_token_bytes(case)
     qo = 2 * case.q.numel() * e
     tbl = int(sum(-(-int(L) // s.bs) for L in lens)) * 4 + 4 * len(lens)
     return kv + qo + tbl
@@ -373,7 +420,7 @@ def unique_decode_bytes(case):
             valid = min(s.bs, int(L) - j * s.bs)
             blk = int(tables[b, j])
             seen[blk] = max(seen.get(blk, 0), valid)
-    kv = sum(seen.values()) * 2 * s.Hkv * s.D * e
+    kv = sum(seen.values()) * _kv_token_bytes(case)
     qo = 2 * case.q.numel() * e
     tbl = int(sum(-(-int(L) // s.bs) for L in lens)) * 4 + 4 * len(lens)
     return kv + qo + tbl
@@ -382,5 +429,7 @@ def unique_decode_bytes(case):
 def append_bytes(case):
     """Bytes the KV append must move: read key/value rows, write them."""
     T = int((case.slot_mapping >= 0).sum())
-    row = case.spec.Hkv * case.spec.D * case.key.element_size()
-    return 2 * 2 * T * row + 8 * case.slot_mapping.numel()
+    n = case.spec.Hkv * case.spec.D
+    if case.extra.get("kv") == "fp8":       # bf16/fp32 rows in, codes and scales out
+        return 2 * T * (n * case.key.element_size() + n + 4) + 8 * case.slot_mapping.numel()
+    return 2 * 2 * T * n * case.key.element_size() + 8 * case.slot_mapping.numel()

@@ -66,6 +66,18 @@ def test_host_side_rejections_launch_nothing(pa):
     assert L.pa_swap_blocks(fake, fake, 4, null, fake, 10, fake, 2, 16, 2, 64, 1, null) == -1
     assert L.pa_swap_blocks(odd, fake, 4, fake, fake, 10, fake, 2, 16, 2, 64, 1, null) == -4
     assert L.pa_swap_blocks(fake, fake, 4, fake, fake, 10, fake, 2, 12, 2, 64, 1, null) == -2
+    # e4m3 pools: fp32 queries are not supported, scales are required and aligned
+    assert L.pa_decode_fp8(fake, fake, fake, fake, fake, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0, 0,
+                           null, 0, 0, null) == -3
+    assert L.pa_decode_fp8(fake, fake, fake, fake, null, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0, 0,
+                           null, 0, 1, null) == -1
+    assert L.pa_decode_fp8(fake, fake, fake, fake, odd, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0, 0,
+                           null, 0, 1, null) == -4
+    assert L.pa_reshape_and_cache_fp8(fake, fake, fake, 3, fake, fake, null, fake, 10, 16, 2, 64, 1, null) == -1
+    assert L.pa_reshape_and_cache_fp8(fake, fake, fake, 3, fake, fake, fake, fake, 10, 16, 2, 64, 2, null) == -3
+    # copies accept e4m3 pools and the [NB, bs, 1, 1] fp32 scale rows, not blocks of a partial chunk
+    assert L.pa_copy_blocks(fake, fake, fake, 0, 10, 16, 1, 1, 0, null) == 0
+    assert L.pa_copy_blocks(fake, fake, fake, 0, 10, 4, 1, 1, 2, null) == -2      # 4 bytes per block
     # empty inputs are a no-op success
     assert L.pa_copy_blocks(null, null, null, 0, 10, 16, 2, 64, 1, null) == 0
     assert L.pa_swap_blocks(null, null, 4, null, null, 10, null, 0, 16, 2, 64, 1, null) == 0
