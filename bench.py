@@ -76,7 +76,19 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel_src, workload):
+def kernel_hash(paths):
+    """sha256 over the decode kernel's source files, in order."""
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
+DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_307_gb300", "csrc", f)
+                  for f in ("pa_decode_kernel.cuh", "pa_decode.cu")]
+
+
+def traffic_record(workload):
     """ncu DRAM bytes per launch of the decode kernel, from a committed
     profile summary; None if it is missing or the kernel changed since."""
     p = os.path.join(ROOT, "profiles", "decode_%s_traffic.json" % workload)
@@ -84,7 +96,7 @@ def traffic_record(kernel_src, workload):
         d = json.load(open(p))
     except Exception:
         return None
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    h = kernel_hash(DECODE_SOURCES)
     return d.get("traffic_bytes_per_launch") if d.get("kernel_sha256") == h else None
 
 
@@ -743,8 +755,7 @@ def run_ours(args, rank, world, local_rank):
         return
     peak, peak_src = peaks()
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_307_gb300", "csrc", "pa_decode.cu"),
-                             args.workload)
+    traffic = traffic_record(args.workload)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),

@@ -12,20 +12,30 @@
 //    128/G positions x G query heads (GQA packing), so every K/V tile is
 //    loaded once for all G heads.  D = 128.
 //  * Warp 0 (TMA): the Q tile (two 64-column halves, 128-byte swizzle) once,
-//    then per 128-key tile the K and V rows of each physical block (box {64,
-//    1 head, bs, 1 block} per half) into a 2-stage ring.  Warp 1 (MMA):
-//    allocates 256 TMEM columns and issues, per key tile, S = Q K^T
-//    (M = N = 128, K = 128: 8 tcgen05.mma) into TMEM columns 0..127 and, once
-//    the softmax has written P, O += P V (V as an MN-major operand) into
-//    columns 128..255.  Warps 2-5 (softmax): one thread per row loads its S
-//    row from TMEM, applies the causal mask and scale (base 2), keeps a
-//    running max and sum, writes P = exp2(s - m) as bf16 into shared memory
-//    in the operand's swizzled layout, and at the end reads O back, divides
-//    by the sum and stores bf16 rows.
+//    then per 64-key tile the K and V rows of its physical blocks (box {64,
+//    1 head, bs, 1 block} per half) into a 2-stage ring; lane 0 arms the
+//    stage's mbarrier and the tile's loads are issued by parallel lanes (one
+//    warp instruction), since one thread issuing them in series was slow.
+//  * Warp 1 (MMA): allocates 256 TMEM columns (S buffers at columns 0 and 64,
+//    O at 128..255) and issues S_{j+1} = Q K_{j+1}^T (M = 128, N = 64,
+//    K = 128: 8 tcgen05.mma) before waiting for P_j, so the next tile's
+//    scores are computed while the softmax works on this one; then
+//    O += P_j V_j with P read from TMEM (the .kind::f16 form whose A operand
+//    is in tensor memory; V is an MN-major shared-memory operand).  Each
+//    group of MMAs completes on an mbarrier through tcgen05.commit; MMAs and
+//    commits execute in issue order, which is what makes reusing an S
+//    buffer (and the P written over it) safe two tiles later.
+//  * Warps 2-5 (softmax): one thread per row loads its 64 scores from TMEM
+//    (tcgen05.ld 32x32b), applies the causal mask and scale (base 2), keeps
+//    a running max and sum, and writes P = exp2(s - m) back as packed bf16
+//    over the first 32 columns of the same S buffer (tcgen05.st); at the end
+//    it reads O back, divides by the sum and stores bf16 rows.
+//  * 98 KB of shared memory and 192 threads per CTA: two CTAs per SM, so one
+//    CTA's softmax overlaps the other's MMAs.
 //  * The running max used as the exponent reference only moves when a new
 //    maximum exceeds it by more than 2^8; then the row's O is rescaled in
-//    TMEM.  The sum and O always share the same reference, so the final
-//    quotient is exact up to rounding.
+//    TMEM (after the previous P V has completed).  The sum and O always share
+//    the same reference, so the final quotient is exact up to rounding.
 //  * V rows at keys >= L (the unfilled tail of the last block, or blocks not
 //    loaded) are zeroed in shared memory before P V reads them: those slots
 //    may hold anything, and 0 * NaN would poison the product.
