@@ -20,10 +20,21 @@ namespace {
 
 // ------------------------------------------------------------------ host side
 
-// CUDA-core variant (HG = 1): KT is the pool's element type.
-template <typename T, typename KT, int D, int GT>
+// Launch-shape parameters of the CUDA-core path (compile-time defaults).
+#ifndef PA_FFMA_STAGE_BUDGET
+#define PA_FFMA_STAGE_BUDGET 65536    // bytes of K/V stages per CTA
+#endif
+#ifndef PA_MAX_STAGES_PER_GROUP
+#define PA_MAX_STAGES_PER_GROUP 4
+#endif
+#ifndef PA_MHA_HEADS_PER_ITEM
+#define PA_MHA_HEADS_PER_ITEM 1       // bf16 pools, head_dim 128, one query head per KV head
+#endif
+
+// CUDA-core variant: KT is the pool's element type, HG KV heads per item.
+template <typename T, typename KT, int D, int GT, int HG = 1>
 Launch pick3() {
-  return {reinterpret_cast<const void*>(&decode_kernel<T, KT, D, GT, false, 1>),
+  return {reinterpret_cast<const void*>(&decode_kernel<T, KT, D, GT, false, HG>),
           reinterpret_cast<const void*>(&merge_kernel<T, D>)};
 }
 
@@ -46,17 +57,19 @@ Launch pick_mma(int gt, int hg) {
 }
 
 template <typename T, typename KT, int D>
-Launch pick2(int gt) {
+Launch pick2(int gt, int hg) {
   if (gt == 4) return pick3<T, KT, D, 4>();
   if (gt == 2) return pick3<T, KT, D, 2>();
+  if constexpr (PA_MHA_HEADS_PER_ITEM > 1 && D == 128 && sizeof(T) == 2)
+    if (hg == PA_MHA_HEADS_PER_ITEM) return pick3<T, KT, D, 1, PA_MHA_HEADS_PER_ITEM>();
   return pick3<T, KT, D, 1>();
 }
 
 template <typename T, typename KT>
-Launch pick1(int d, int gt) {
-  if (d == 32) return pick2<T, KT, 32>(gt);
-  if (d == 64) return pick2<T, KT, 64>(gt);
-  return pick2<T, KT, 128>(gt);
+Launch pick1(int d, int gt, int hg) {
+  if (d == 32) return pick2<T, KT, 32>(gt, hg);
+  if (d == 64) return pick2<T, KT, 64>(gt, hg);
+  return pick2<T, KT, 128>(gt, hg);
 }
 
 struct KernelInfo {
@@ -219,9 +232,12 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   // KV heads per work item: 4 on the tensor-core path (one warp per head,
   // the four heads' tiles loaded back to back); 1 on the CUDA-core path,
   // where a warp ring per head measured faster for MHA.
+  const bool mha_hg = kv == PA_BF16 && head_dim == 128 && G == 1 && PA_MHA_HEADS_PER_ITEM > 1 &&
+                      num_kv_heads % PA_MHA_HEADS_PER_ITEM == 0;
   const int HG = use_mma ? (num_kv_heads % 4 == 0 ? 4 : num_kv_heads % 2 == 0 ? 2 : 1)
-                 : fp8   ? fp8_heads_per_item(num_kv_heads)
-                         : 1;
+                 : fp8    ? fp8_heads_per_item(num_kv_heads)
+                 : mha_hg ? PA_MHA_HEADS_PER_ITEM
+                          : 1;
   if (!get_map(&mapK, k_cache, kv, num_blocks, block_size, num_kv_heads, head_dim, dev, use_mma, HG) ||
       !get_map(&mapV, v_cache, kv, num_blocks, block_size, num_kv_heads, head_dim, dev, use_mma, HG)) {
     note_host_error("cuTensorMapEncodeTiled failed for the K/V pool");
@@ -253,6 +269,7 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   prm.n_hg = num_kv_heads / prm.HG;
   prm.WPH = kConsumerWarps / prm.HG;
   prm.n_virtual = (long long)max_parts * prm.nsub * prm.n_hg * num_seqs;
+  prm.dense = num_seqs <= kDenseMaxSeqs ? 1 : 0;
   prm.qscale = scale * kLog2e;
   prm.k_scale = fp8 ? k_scale : nullptr;
   prm.v_scale = fp8 ? v_scale : nullptr;
@@ -261,24 +278,27 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   // the four head warps), ~64 KB on the CUDA-core path (a ring per warp);
   // 1..4 stages per warp group.  A shared ring keeps at least 2 stages, and
   // when its stages are so large that one CTA fills the SM anyway, 3.
-  const int budget = use_mma ? 98304 : 65536;
+  const int budget = use_mma ? 98304 : PA_FFMA_STAGE_BUDGET;
   int spg = (int)(budget / (2 * prm.tile_bytes * kConsumerWarps));
-  spg = spg < 1 ? 1 : (spg > 4 ? 4 : spg);
+  spg = spg < 1 ? 1 : (spg > PA_MAX_STAGES_PER_GROUP ? PA_MAX_STAGES_PER_GROUP : spg);
+  while (!use_mma && (spg & (spg - 1))) spg &= spg - 1;   // CUDA-core path: a power of two
   if (prm.WPH == 1) {
     const size_t stage = 2 * (size_t)prm.HG * prm.tile_bytes;
     if (spg < 2) spg = 2;
     if ((size_t)spg * stage > 102400 && 3 * stage <= 200 * 1024) spg = 3;
   }
   prm.spg = spg;
+  prm.spg_shift = (spg & (spg - 1)) ? -1 : (spg == 1 ? 0 : spg == 2 ? 1 : spg == 4 ? 2 : 3);
   const int S = spg * prm.WPH;
 
   const Launch L = use_mma ? (head_dim == 64 ? pick_mma<64>(GT, prm.HG) : pick_mma<128>(GT, prm.HG))
                    : fp8             ? pick_decode_fp8(head_dim, GT, prm.HG)
-                   : dtype == PA_F32 ? pick1<float, float>(head_dim, GT)
-                                     : pick1<__nv_bfloat16, __nv_bfloat16>(head_dim, GT);
+                   : dtype == PA_F32 ? pick1<float, float>(head_dim, GT, prm.HG)
+                                     : pick1<__nv_bfloat16, __nv_bfloat16>(head_dim, GT, prm.HG);
   const size_t smem = 2 * (size_t)S * prm.HG * prm.tile_bytes + (fp8 ? 2 * (size_t)S * block_size * 4 : 0) +
                       (size_t)kConsumerWarps * GT * (head_dim + 2) * sizeof(float) +
-                      2 * (size_t)S * sizeof(uint64_t) + 16 + kSmemAlign;
+                      2 * (size_t)S * sizeof(uint64_t) + 16 +
+                      (prm.dense ? 4 * (2 * (size_t)num_seqs + 1 + kThreads / 32) : 0) + kSmemAlign;
   const int occ = occupancy_for(L.kernel, smem, dev);
   if (occ <= 0) return PA_ERR_CUDA;
   long long grid = (long long)occ * device_sm_count();

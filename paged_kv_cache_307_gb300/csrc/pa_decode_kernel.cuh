@@ -66,6 +66,7 @@ struct DecodeParams {
   int max_blocks, bs, num_blocks;
   int part_tokens, max_parts;
   long long n_virtual;
+  int dense;          // 1: enumerate only real items through a per-CTA prefix table (B <= kDenseMaxSeqs)
   float qscale;       // scale * log2(e)
   const float* k_scale;  // e4m3 pools: per-token K scales [num_blocks * bs]; else null
   const float* v_scale;  // e4m3 pools: per-token V scales
@@ -73,6 +74,7 @@ struct DecodeParams {
   int n_hg;           // Hkv / HG
   int WPH;            // warp groups: kConsumerWarps / HG (warps sharing one head)
   int spg;            // shared-memory stages per warp group
+  int spg_shift;      // log2(spg) when spg is a power of two, else -1
   uint32_t tile_bytes;  // one head's K (or V) tile of one block: bs * D * elem
 };
 
@@ -102,6 +104,42 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Sequences up to which items are enumerated densely: each CTA keeps the
+// clamped lengths and the prefix sum of partitions per sequence in shared
+// memory (8 bytes per sequence).
+constexpr int kDenseMaxSeqs = 1024;
+
+__device__ __forceinline__ void finish_item(const DecodeParams& p, int L, int nparts, Item& it) {
+  const int t0 = it.part * p.part_tokens;
+  it.t1 = min(L, t0 + p.part_tokens);
+  it.jb = t0 / p.bs;
+  it.je = (it.t1 + p.bs - 1) / p.bs;
+  if (it.je < it.jb) it.je = it.jb;
+  it.split = nparts > 1;
+}
+
+// Dense item i -> (sequence, partition, KV-head group, query subgroup): the
+// (sequence, partition) units are numbered sequence by sequence, and the
+// n_hg * nsub items of a unit are consecutive, so the CTAs running side by
+// side cover neighbouring sequences (siblings sharing a prompt read the same
+// blocks) and every CTA gets the same number of items up to one.
+__device__ __forceinline__ void dense_item(const DecodeParams& p, const int* pre, const int* Ls, int i, Item& it) {
+  const int nper = p.n_hg * p.nsub;
+  const int u = i / nper;
+  const int r = i - u * nper;
+  it.kvh0 = (r % p.n_hg) * p.HG;
+  it.sg = r / p.n_hg;
+  int lo = 0, hi = p.B - 1;       // the last sequence whose first unit is <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  it.b = lo;
+  it.part = u - pre[lo];
+  finish_item(p, Ls[lo], pre[lo + 1] - pre[lo], it);
+}
+
 __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, Item& it) {
   it.b = (int)(v % p.B);
   long long r = v / p.B;
@@ -114,12 +152,7 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, 
   if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;   // flagged by the consumer
   const int nparts = L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
   if (it.part >= nparts) return false;
-  const int t0 = it.part * p.part_tokens;
-  it.t1 = min(L, t0 + p.part_tokens);
-  it.jb = t0 / p.bs;
-  it.je = (it.t1 + p.bs - 1) / p.bs;
-  if (it.je < it.jb) it.je = it.jb;
-  it.split = nparts > 1;
+  finish_item(p, L, nparts, it);
   return true;
 }
 
@@ -166,6 +199,10 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + NCW * GT * (D + 2));
   uint64_t* empty = full + S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  // dense enumeration: partition prefix [B+1], clamped lengths [B], warp sums
+  int* pre = const_cast<int*>(abort_flag) + 4;
+  int* Ls = pre + (p.dense ? p.B + 1 : 0);
+  int* wsum = Ls + (p.dense ? p.B : 0);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -178,7 +215,40 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  long long n_items = p.n_virtual;
+  if (p.dense) {
+    // Every CTA builds the same tables: each thread takes a contiguous run
+    // of sequences, then a block-wide exclusive scan of the run totals.
+    const int Lmax = p.max_blocks * p.bs;
+    const int per = (p.B + kThreads - 1) / kThreads;
+    const int b0 = min(p.B, (int)threadIdx.x * per), b1 = min(p.B, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      int L = __ldg(&p.context_lens[b]);
+      if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;   // flagged by the consumer
+      Ls[b] = L;
+      sum += L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int b = b0; b < b1; ++b) {
+      pre[b] = run;
+      run += Ls[b] > 0 ? (Ls[b] + p.part_tokens - 1) / p.part_tokens : 1;
+    }
+    if (threadIdx.x == kThreads - 1) pre[p.B] = run;
+    __syncthreads();
+    n_items = (long long)pre[p.B] * p.n_hg * p.nsub;
+  } else {
+    __syncthreads();
+  }
 
   // An item covers HG KV heads.  Consumer warp w works on head w % HG of
   // the item, in warp group w / HG; block i of the item goes to group
@@ -190,6 +260,18 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   // every role); stage = g*SPW + u % SPW.  The HG heads of a block are loaded
   // back to back, so the DRAM sees neighbouring rows of the pool together.
   const int SPW = p.spg;
+  // Running block count u of a group -> (stage within the group's ring,
+  // phase parity).  Shifts when the ring depth is a power of two: a runtime
+  // division here costs a noticeable share of the producer's per-block work.
+  const int spw_shift = p.spg_shift;
+  auto ring = [SPW, spw_shift](uint32_t u, uint32_t& ph) -> int {
+    if (spw_shift >= 0) {
+      ph = (u >> spw_shift) & 1u;
+      return (int)(u & (uint32_t)(SPW - 1));
+    }
+    ph = (u / (uint32_t)SPW) & 1u;
+    return (int)(u % (uint32_t)SPW);
+  };
 
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
@@ -204,9 +286,10 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     uint32_t base[NCW], issued[NCW];
 #pragma unroll
     for (int w = 0; w < NCW; ++w) base[w] = issued[w] = 0;
-    for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
+    for (long long v = blockIdx.x; v < n_items; v += gridDim.x) {
       Item item;
-      if (!decode_item(p, v, item)) continue;
+      if (p.dense) dense_item(p, pre, Ls, (int)v, item);
+      else if (!decode_item(p, v, item)) continue;
       const int32_t* row = p.block_tables + (size_t)item.b * p.max_blocks;
       const int nblk = item.je - item.jb;
       for (int j0 = 0; j0 < nblk; j0 += 32) {
@@ -226,8 +309,8 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < WPH; ++k)
             if (k == w) u = base[k] + (uint32_t)((j0 + i) / WPH);
-          const int st = w * SPW + (int)(u % SPW);
-          const uint32_t ph = (u / SPW) & 1u;
+          uint32_t ph;
+          const int st = w * SPW + ring(u, ph);
           constexpr int HALVES = MMA ? D / 64 : 1;
           constexpr int NOPS = MMA ? 2 * HG * HALVES : 2;   // TMA loads per block
           int go = 0;
@@ -238,23 +321,28 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             } else {
               mbar_arrive_expect_tx(&full[st], 2u * stage_bytes + (SCALED ? 8u * (uint32_t)p.bs : 0u));
               go = 1;
-              if constexpr (NOPS == 2) {
-                // one box {D, HG heads, bs, 1} each for K and V: smem [bs][HG][D]
-                tma_load_4d(tilesK + (size_t)st * stage_bytes, &mapK, &full[st], 0, item.kvh0, 0, bi, pol);
-                tma_load_4d(tilesV + (size_t)st * stage_bytes, &mapV, &full[st], 0, item.kvh0, 0, bi, pol);
-              }
-              if constexpr (SCALED) {
-                // the block's scale rows: bs fp32 values each, contiguous
-                bulk_load(sclK + st * p.bs, p.k_scale + (size_t)bi * p.bs, 4u * p.bs, &full[st], pol);
-                bulk_load(sclV + st * p.bs, p.v_scale + (size_t)bi * p.bs, 4u * p.bs, &full[st], pol);
-              }
             }
           }
-          if constexpr (NOPS > 2) {
-            // tensor-core path: many 128-byte-swizzled 64-column halves per
-            // block, issued by one warp instruction: lane l takes K (l even)
-            // or V (l odd) of head l/2/HALVES, half l/2%HALVES
-            if (__shfl_sync(0xffffffffu, go, 0) && lane < NOPS) {
+          // The block's copies are issued by parallel lanes in one warp
+          // instruction once lane 0 has armed the stage (one thread issuing
+          // them in series is slower).
+          if (__shfl_sync(0xffffffffu, go, 0)) {
+            if constexpr (NOPS == 2) {
+              // one box {D, HG heads, bs, 1} each for K (lane 0) and V
+              // (lane 1): smem [bs][HG][D]; e4m3 pools also move the block's
+              // two scale rows (bs fp32 values each) from lanes 2 and 3
+              if (lane < 2)
+                tma_load_4d((lane ? tilesV : tilesK) + (size_t)st * stage_bytes, lane ? &mapV : &mapK, &full[st],
+                            0, item.kvh0, 0, bi, pol);
+              if constexpr (SCALED) {
+                if (lane == 2 || lane == 3)
+                  bulk_load((lane == 2 ? sclK : sclV) + st * p.bs,
+                            (lane == 2 ? p.k_scale : p.v_scale) + (size_t)bi * p.bs, 4u * p.bs, &full[st], pol);
+              }
+            } else if (lane < NOPS) {
+              // tensor-core path: many 128-byte-swizzled 64-column halves
+              // per block: lane l takes K (l even) or V (l odd) of head
+              // l/2/HALVES, half l/2%HALVES
               const int rest = lane >> 1;
               const int hl = rest / HALVES, hh = rest % HALVES;
               const size_t off = (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes + (size_t)hh * p.bs * 128;
@@ -294,9 +382,10 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   const int hl = warp % HG;       // the item's KV head this warp works on
   const int gw = warp / HG;       // this warp's group
 
-  for (long long v = blockIdx.x; v < p.n_virtual; v += gridDim.x) {
+  for (long long v = blockIdx.x; v < n_items; v += gridDim.x) {
     Item item;
-    if (!decode_item(p, v, item)) continue;
+    if (p.dense) dense_item(p, pre, Ls, (int)v, item);
+    else if (!decode_item(p, v, item)) continue;
     if (ctid == 0 && item.kvh0 == 0 && item.sg == 0 && item.part == 0) {
       const int L = __ldg(&p.context_lens[item.b]);
       if (L < 0 || L > p.max_blocks * p.bs) atomicOr(&g_status_decode, PA_DEV_BAD_LEN);
@@ -333,8 +422,8 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 
       const int nblk = item.je - item.jb;
       for (int i = gw; i < nblk; i += WPH, ++wcount) {
-        const int st = gw * SPW + (int)(wcount % SPW);
-        const uint32_t ph = (wcount / SPW) & 1u;
+        uint32_t ph;
+        const int st = gw * SPW + ring(wcount, ph);
         bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
         if (live) {
           const bool late = !mbar_wait(&full[st], ph);
@@ -482,8 +571,8 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 
       const int nblk = item.je - item.jb;
       for (int i = gw; i < nblk; i += WPH, ++wcount) {
-        const int st = gw * SPW + (int)(wcount % SPW);
-        const uint32_t ph = (wcount / SPW) & 1u;
+        uint32_t ph;
+        const int st = gw * SPW + ring(wcount, ph);
         bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
         if (live) {
           const bool late = !mbar_wait(&full[st], ph);
