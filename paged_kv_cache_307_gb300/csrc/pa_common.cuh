@@ -165,12 +165,20 @@ template <> struct Elem<__nv_bfloat16> {
 struct fp8e4m3 {
   uint8_t bits;
 };
-// Two e4m3 codes (low byte = first element) to two floats, exactly.
-__device__ __forceinline__ void e4m3x2_to_float2(uint32_t two, float& lo, float& hi) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  lo = f.x;
-  hi = f.y;
+// Four e4m3 codes (byte i = element i) to two f16x2 values (elements 0,1
+// and 2,3), exactly: every e4m3 value is an f16 value.  The 32-bit word is
+// split into its 16-bit halves and each is converted by one instruction.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+// An f16x2 value to two floats, exactly.
+__device__ __forceinline__ void f16x2_to_float2(uint32_t h, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
 }
 template <> struct Elem<fp8e4m3> {
   static constexpr int kBytes = 1;
@@ -179,8 +187,10 @@ template <> struct Elem<fp8e4m3> {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      e4m3x2_to_float2(w[i], f[4 * i], f[4 * i + 1]);
-      e4m3x2_to_float2(w[i] >> 16, f[4 * i + 2], f[4 * i + 3]);
+      uint32_t h01, h23;
+      e4m3x4_to_f16x2x2(w[i], h01, h23);
+      f16x2_to_float2(h01, f[4 * i], f[4 * i + 1]);
+      f16x2_to_float2(h23, f[4 * i + 2], f[4 * i + 3]);
     }
   }
 };

@@ -105,7 +105,7 @@ bool get_map(CUtensorMap* out, const void* base, pa_dtype dt, int nb, int bs, in
     const uint64_t e = (uint64_t)elem_bytes(dt);
     const uint64_t dims[4] = {(uint64_t)d, (uint64_t)h, (uint64_t)bs, (uint64_t)nb};
     const uint64_t str[3] = {d * e, (uint64_t)h * d * e, (uint64_t)bs * h * d * e};
-    const uint32_t box[4] = {64, 1, (uint32_t)bs, 1};
+    const uint32_t box[4] = {(uint32_t)(128 / e), 1, (uint32_t)bs, 1};   // one 128-byte row span
     ok = encode_map(out, base, dt, 4, dims, str, box, true);
   } else {
     const uint64_t e = (uint64_t)elem_bytes(dt);
@@ -143,7 +143,7 @@ int occupancy_for(const void* kernel, size_t smem, int dev) {
 #define PA_FP8_HEADS_PER_ITEM 2
 #endif
 int fp8_heads_per_item(int num_kv_heads) {
-  int hg = PA_FP8_HEADS_PER_ITEM;
+  int hg = PA_FP8_HEADS_PER_ITEM > 2 ? 2 : PA_FP8_HEADS_PER_ITEM;   // instances: 1 or 2
   while (hg > 1 && num_kv_heads % hg) hg >>= 1;
   return hg;
 }
@@ -227,14 +227,20 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   CUtensorMap mapK, mapV;
   const int G = num_heads / num_kv_heads;
   // Tensor cores over the query group when it is a real contraction (G >= 2).
-  const bool use_mma = kv == PA_BF16 && (head_dim == 64 || head_dim == 128) && G >= 2 && (G & (G - 1)) == 0 &&
-                       block_size >= 8;
+  const bool use_mma = ((kv == PA_BF16 && (head_dim == 64 || head_dim == 128)) ||
+                        (kv == PA_FP8_E4M3 && head_dim == 128)) &&
+                       G >= 2 && (G & (G - 1)) == 0 && block_size >= 8;
   // KV heads per work item: 4 on the tensor-core path (one warp per head,
   // the four heads' tiles loaded back to back); 1 on the CUDA-core path,
   // where a warp ring per head measured faster for MHA.
   const bool mha_hg = kv == PA_BF16 && head_dim == 128 && G == 1 && PA_MHA_HEADS_PER_ITEM > 1 &&
                       num_kv_heads % PA_MHA_HEADS_PER_ITEM == 0;
-  const int HG = use_mma ? (num_kv_heads % 4 == 0 ? 4 : num_kv_heads % 2 == 0 ? 2 : 1)
+// KV heads per item on the e4m3 tensor-core path (2 measured fastest).
+#ifndef PA_FP8_MMA_HG
+#define PA_FP8_MMA_HG 2
+#endif
+  const int hg_mma = fp8 ? PA_FP8_MMA_HG : 4;
+  const int HG = use_mma ? (num_kv_heads % hg_mma == 0 ? hg_mma : num_kv_heads % 2 == 0 ? 2 : 1)
                  : fp8    ? fp8_heads_per_item(num_kv_heads)
                  : mha_hg ? PA_MHA_HEADS_PER_ITEM
                           : 1;
@@ -291,8 +297,8 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   prm.spg_shift = (spg & (spg - 1)) ? -1 : (spg == 1 ? 0 : spg == 2 ? 1 : spg == 4 ? 2 : 3);
   const int S = spg * prm.WPH;
 
-  const Launch L = use_mma ? (head_dim == 64 ? pick_mma<64>(GT, prm.HG) : pick_mma<128>(GT, prm.HG))
-                   : fp8             ? pick_decode_fp8(head_dim, GT, prm.HG)
+  const Launch L = fp8               ? pick_decode_fp8(head_dim, GT, prm.HG, use_mma)
+                   : use_mma         ? (head_dim == 64 ? pick_mma<64>(GT, prm.HG) : pick_mma<128>(GT, prm.HG))
                    : dtype == PA_F32 ? pick1<float, float>(head_dim, GT, prm.HG)
                                      : pick1<__nv_bfloat16, __nv_bfloat16>(head_dim, GT, prm.HG);
   const size_t smem = 2 * (size_t)S * prm.HG * prm.tile_bytes + (fp8 ? 2 * (size_t)S * block_size * 4 : 0) +

@@ -13,11 +13,12 @@
 namespace pa {
 namespace {
 
+using B16 = __nv_bfloat16;
+
+// CUDA-core instances: 1 or 2 KV heads per item.
 template <int D, int GT>
 Launch pick_hg(int hg) {
-  using B16 = __nv_bfloat16;
   const void* merge = reinterpret_cast<const void*>(&merge_kernel<B16, D>);
-  if (hg == 4) return {reinterpret_cast<const void*>(&decode_kernel<B16, fp8e4m3, D, GT, false, 4>), merge};
   if (hg == 2) return {reinterpret_cast<const void*>(&decode_kernel<B16, fp8e4m3, D, GT, false, 2>), merge};
   return {reinterpret_cast<const void*>(&decode_kernel<B16, fp8e4m3, D, GT, false, 1>), merge};
 }
@@ -29,9 +30,24 @@ Launch pick_gt(int gt, int hg) {
   return pick_hg<D, 1>(hg);
 }
 
+// Tensor-core instances (head_dim 128): GT query heads per KV head, HG KV heads per item.
+template <int GT>
+Launch pick_mma_hg(int hg) {
+  const void* merge = reinterpret_cast<const void*>(&merge_kernel<B16, 128>);
+  if (hg == 4) return {reinterpret_cast<const void*>(&decode_kernel<B16, fp8e4m3, 128, GT, true, 4>), merge};
+  if (hg == 2) return {reinterpret_cast<const void*>(&decode_kernel<B16, fp8e4m3, 128, GT, true, 2>), merge};
+  return {reinterpret_cast<const void*>(&decode_kernel<B16, fp8e4m3, 128, GT, true, 1>), merge};
+}
+
 }  // namespace
 
-Launch pick_decode_fp8(int head_dim, int gt, int hg) {
+Launch pick_decode_fp8(int head_dim, int gt, int hg, bool mma) {
+  if (mma) {
+    if (gt == 16) return pick_mma_hg<16>(hg);
+    if (gt == 8) return pick_mma_hg<8>(hg);
+    if (gt == 4) return pick_mma_hg<4>(hg);
+    return pick_mma_hg<2>(hg);
+  }
   if (head_dim == 32) return pick_gt<32>(gt, hg);
   if (head_dim == 64) return pick_gt<64>(gt, hg);
   return pick_gt<128>(gt, hg);

@@ -99,6 +99,18 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
 }
+// m16n8k16 f16 tensor-core product with fp32 accumulation (per warp).
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -158,8 +170,14 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, 
 
 // T: query/output element type; KT: K/V pool element type (T itself, or
 // e4m3 codes with a per-token scale for K and for V).
+// e4m3 tensor-core instances are held to three CTAs per SM (at most 136
+// registers): their per-block conversion work needs the extra warps to hide
+// latency (20 % faster on the grouped-query workload than two CTAs per SM).
+#ifndef PA_FP8_MMA_MIN_BLOCKS
+#define PA_FP8_MMA_MIN_BLOCKS 3
+#endif
 template <typename T, typename KT, int D, int GT, bool MMA, int HG>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (MMA && sizeof(KT) == 1) ? PA_FP8_MMA_MIN_BLOCKS : 1)
 decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const DecodeParams p) {
   using E = Elem<T>;                           // queries and output
@@ -180,7 +198,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   constexpr int NCW = kConsumerWarps;
   static_assert(LPT >= 1 && LPT <= 32 && (32 % LPT) == 0, "lane split");
   static_assert(QPC >= 1 && EPC % E::kPerChunk == 0, "query chunking");
-  static_assert(!(SCALED && MMA), "e4m3 pools use the CUDA-core path");
+  static_assert(!(SCALED && MMA) || D == 128, "e4m3 tensor-core path: head_dim 128");
 
   constexpr int WPH = kConsumerWarps / HG;               // warp groups (warps sharing a head)
   static_assert(HG == 1 || HG == 2 || HG == 4, "KV heads per item");
@@ -311,7 +329,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
             if (k == w) u = base[k] + (uint32_t)((j0 + i) / WPH);
           uint32_t ph;
           const int st = w * SPW + ring(u, ph);
-          constexpr int HALVES = MMA ? D / 64 : 1;
+          constexpr int HALVES = MMA ? D * EK::kBytes / 128 : 1;   // 128-byte swizzled column spans
           constexpr int NOPS = MMA ? 2 * HG * HALVES : 2;   // TMA loads per block
           int go = 0;
           if (lane == 0 && !*abort_flag) {
@@ -340,14 +358,19 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                             (lane == 2 ? p.k_scale : p.v_scale) + (size_t)bi * p.bs, 4u * p.bs, &full[st], pol);
               }
             } else if (lane < NOPS) {
-              // tensor-core path: many 128-byte-swizzled 64-column halves
-              // per block: lane l takes K (l even) or V (l odd) of head
-              // l/2/HALVES, half l/2%HALVES
+              // tensor-core path: many 128-byte-swizzled column spans per
+              // block (64 bf16 or 128 e4m3 columns): lane l takes K (l even)
+              // or V (l odd) of head l/2/HALVES, span l/2%HALVES
               const int rest = lane >> 1;
               const int hl = rest / HALVES, hh = rest % HALVES;
               const size_t off = (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes + (size_t)hh * p.bs * 128;
               unsigned char* dst = ((lane & 1) ? tilesV : tilesK) + off;
-              tma_load_4d(dst, (lane & 1) ? &mapV : &mapK, &full[st], hh * 64, item.kvh0 + hl, 0, bi, pol);
+              tma_load_4d(dst, (lane & 1) ? &mapV : &mapK, &full[st], hh * (128 / EK::kBytes), item.kvh0 + hl, 0,
+                          bi, pol);
+            } else if (SCALED && (lane == NOPS || lane == NOPS + 1)) {
+              const bool vs = lane == NOPS + 1;
+              bulk_load((vs ? sclV : sclK) + st * p.bs, (vs ? p.v_scale : p.k_scale) + (size_t)bi * p.bs, 4u * p.bs,
+                        &full[st], pol);
             }
           }
           if (lane == 0 && go) {
@@ -392,7 +415,239 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
     const int h0 = (item.kvh0 + hl) * p.G + item.sg * GT;
 
-    if constexpr (MMA) {
+    if constexpr (MMA && SCALED) {
+      // e4m3 pool on tensor cores (f16 m16n8k16, fp32 accumulation), the
+      // query group in the M rows as on the bf16 path.  Differences:
+      //  * K codes are read with ldmatrix as byte pairs: a lane gets 4
+      //    consecutive codes (head dims 4tq..4tq+3 of a 16-dim chunk) of one
+      //    token, converted exactly to two f16x2 values.  The reduction
+      //    index of each k-step is permuted the same way in the Q fragment
+      //    (slots 2tq,2tq+1 <-> dims 4tq,4tq+1; slots 2tq+8,2tq+9 <-> dims
+      //    4tq+2,4tq+3), which leaves Q K^T unchanged.
+      //  * Q is converted to f16 after a per-item power-of-two scaling that
+      //    puts its largest magnitude in [2^14, 2^15), so the conversion is
+      //    exact for every value within 2^-28 of that maximum; the scores
+      //    get the inverse power of two with the softmax scale, and each
+      //    token's K scale.
+      //  * V codes are read with ldmatrix.trans as byte pairs; one byte
+      //    permute splits a lane's 4 codes into its even-dim and odd-dim
+      //    pairs, so each 16-dim chunk gives two n-tiles (even dims, odd
+      //    dims) of the output.
+      //  * P carries the token's V scale relative to a running power-of-two
+      //    reference 2^rexp (the largest V scale seen, rounded up), so the
+      //    f16 P stays in [0, 1]; O is rescaled when the reference grows and
+      //    multiplied back by 2^rexp at the end.  The softmax sum uses the
+      //    unscaled weights.
+      constexpr int KS = D / 16;       // k-steps of Q K^T
+      constexpr int NT = D / 8;        // output n-tiles (two per 16-dim chunk)
+      const int g = lane >> 2, tq = lane & 3;
+      const bool r0v = g < GT, r1v = g + 8 < GT;
+      const uint2* q0p = reinterpret_cast<const uint2*>(
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + (r0v ? g : 0)) * QROW);
+      const uint2* q1p = reinterpret_cast<const uint2*>(
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + (r1v ? g + 8 : 0)) * QROW);
+      uint2 qraw[KS][2];
+      float qmax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qraw[kk][0] = r0v ? __ldg(q0p + kk * 4 + tq) : make_uint2(0u, 0u);   // dims 16kk+4tq .. +3
+        qraw[kk][1] = r1v ? __ldg(q1p + kk * 4 + tq) : make_uint2(0u, 0u);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          qmax = fmaxf(qmax, fmaxf(fabsf(bf16lo(qraw[kk][r].x)), fabsf(bf16hi(qraw[kk][r].x))));
+          qmax = fmaxf(qmax, fmaxf(fabsf(bf16lo(qraw[kk][r].y)), fabsf(bf16hi(qraw[kk][r].y))));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+      // 2^qe >= qmax / 2^15, so |q| * 2^-qe <= 2^15 < 65504
+      int qe = 0;
+      if (qmax > 0.f) qe = max(-100, min(100, ilogbf(qmax) - 14));
+      const float qdown = ldexpf(1.f, -qe);
+      uint32_t qa[KS][4];
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qa[kk][0] = pack_f16(bf16lo(qraw[kk][0].x) * qdown, bf16hi(qraw[kk][0].x) * qdown);
+        qa[kk][1] = pack_f16(bf16lo(qraw[kk][1].x) * qdown, bf16hi(qraw[kk][1].x) * qdown);
+        qa[kk][2] = pack_f16(bf16lo(qraw[kk][0].y) * qdown, bf16hi(qraw[kk][0].y) * qdown);
+        qa[kk][3] = pack_f16(bf16lo(qraw[kk][1].y) * qdown, bf16hi(qraw[kk][1].y) * qdown);
+      }
+      const float sfac = p.qscale * ldexpf(1.f, qe);
+      float O[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
+      float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};
+      int rexp = -1000;                // V-scale reference exponent (none yet)
+
+      const int nblk = item.je - item.jb;
+      for (int i = gw; i < nblk; i += WPH, ++wcount) {
+        uint32_t ph;
+        const int st = gw * SPW + ring(wcount, ph);
+        bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        if (live) {
+          const bool late = !mbar_wait(&full[st], ph);
+          if (__any_sync(0xffffffffu, late)) {
+            live = false;
+            if (lane == 0) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          }
+        }
+        if (live) {
+          const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
+          unsigned char* vt_ptr = tilesV + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
+          const uint32_t kt = smem_u32(tilesK + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes);
+          const uint32_t vt = smem_u32(vt_ptr);
+          const float* sk = sclK + st * p.bs;
+          const float* sv = sclV + st * p.bs;
+          if (valid < p.bs) {
+            // slots past the context may hold anything (NaN codes): clear
+            // those V rows (P is 0 there, but 0 * NaN would be NaN)
+            for (int idx = lane; idx < (p.bs - valid) * 8; idx += 32)
+              *reinterpret_cast<uint4*>(vt_ptr + (valid + idx / 8) * 128 + (idx % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          // V-scale reference for this block (valid tokens only)
+          float vmax = 0.f;
+          for (int t = lane; t < valid; t += 32) vmax = fmaxf(vmax, sv[t]);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+          if (vmax > 0.f) {
+            const int ve = ilogbf(vmax) + 1;          // 2^ve > vmax
+            if (ve > rexp) {
+              if (rexp > -1000) {
+                const float f = ldexpf(1.f, rexp - ve);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                  O[n][0] *= f;
+                  O[n][1] *= f;
+                  O[n][2] *= f;
+                  O[n][3] *= f;
+                }
+              }
+              rexp = ve;
+            }
+          }
+          const float vdown = rexp > -1000 ? ldexpf(1.f, -rexp) : 0.f;
+          for (int tb = 0; tb < valid; tb += 16) {
+            float S[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+              // lanes 0-7: tokens tb..+7, chunk 2kp; 8-15: same tokens,
+              // chunk 2kp+1; 16-31: tokens tb+8..+15, chunks 2kp, 2kp+1
+              const int tt = min(tb + (lane & 7) + ((lane >> 4) << 3), p.bs - 1);
+#pragma unroll
+              for (int kp = 0; kp < KS / 2; ++kp) {
+                const int c = 2 * kp + ((lane >> 3) & 1);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kt + tt * 128 + ((c ^ (tt & 7)) << 4), r0, r1, r2, r3);
+                uint32_t b[4][2];
+                e4m3x4_to_f16x2x2(r0, b[0][0], b[0][1]);
+                e4m3x4_to_f16x2x2(r1, b[1][0], b[1][1]);
+                e4m3x4_to_f16x2x2(r2, b[2][0], b[2][1]);
+                e4m3x4_to_f16x2x2(r3, b[3][0], b[3][1]);
+                mma_f16_16816(S[0], qa[2 * kp], b[0][0], b[0][1]);
+                mma_f16_16816(S[0], qa[2 * kp + 1], b[1][0], b[1][1]);
+                mma_f16_16816(S[1], qa[2 * kp], b[2][0], b[2][1]);
+                mma_f16_16816(S[1], qa[2 * kp + 1], b[3][0], b[3][1]);
+              }
+            }
+            float mx[2] = {-INFINITY, -INFINITY};
+            float vsc[2][2];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int t = tb + n * 8 + 2 * tq + (e & 1);
+                const bool ok = t < valid;
+                S[n][e] = ok ? S[n][e] * (sfac * sk[t]) : -INFINITY;
+                if (e < 2) vsc[n][e] = ok ? sv[t] * vdown : 0.f;
+                mx[e >> 1] = fmaxf(mx[e >> 1], S[n][e]);
+              }
+            float alpha[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+              mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+              const float mn = fmaxf(mr[r], mx[r]);
+              alpha[r] = mn == -INFINITY ? 1.f : exp2f(mr[r] - mn);
+              mr[r] = mn;
+              lr[r] *= alpha[r];
+            }
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+              for (int n = 0; n < NT; ++n) {
+                O[n][0] *= alpha[0];
+                O[n][1] *= alpha[0];
+                O[n][2] *= alpha[1];
+                O[n][3] *= alpha[1];
+              }
+            }
+            float pw[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float pk = (S[n][e] == -INFINITY) ? 0.f : exp2f(S[n][e] - mr[e >> 1]);
+                lr[e >> 1] += pk;
+                pw[n][e] = pk * vsc[n][e & 1];
+              }
+            const uint32_t pa[4] = {pack_f16(pw[0][0], pw[0][1]), pack_f16(pw[0][2], pw[0][3]),
+                                    pack_f16(pw[1][0], pw[1][1]), pack_f16(pw[1][2], pw[1][3])};
+            {
+              // ldmatrix.trans: lanes 0-7 tokens tb..+7, 8-15 tokens tb+8..+15
+              // (chunk 2j); lanes 16-31 the same for chunk 2j+1.  A lane gets
+              // codes (token 2tq: dims 2g, 2g+1; token 2tq+1: dims 2g, 2g+1).
+              const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
+#pragma unroll
+              for (int j = 0; j < D / 32; ++j) {
+                const int c = 2 * j + (lane >> 4);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(vt + tt * 128 + ((c ^ (tt & 7)) << 4), r0, r1, r2, r3);
+                // bytes [b0 b2 | b1 b3]: even-dim pair low, odd-dim pair high
+                uint32_t ev[4], od[4];   // even-dim / odd-dim f16x2 pairs of r0..r3
+                e4m3x4_to_f16x2x2(__byte_perm(r0, 0u, 0x3120), ev[0], od[0]);
+                e4m3x4_to_f16x2x2(__byte_perm(r1, 0u, 0x3120), ev[1], od[1]);
+                e4m3x4_to_f16x2x2(__byte_perm(r2, 0u, 0x3120), ev[2], od[2]);
+                e4m3x4_to_f16x2x2(__byte_perm(r3, 0u, 0x3120), ev[3], od[3]);
+                mma_f16_16816(O[4 * j + 0], pa, ev[0], ev[1]);
+                mma_f16_16816(O[4 * j + 1], pa, od[0], od[1]);
+                mma_f16_16816(O[4 * j + 2], pa, ev[2], ev[3]);
+                mma_f16_16816(O[4 * j + 3], pa, od[2], od[3]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 1);
+        lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
+      }
+      const float vup = rexp > -1000 ? ldexpf(1.f, rexp) : 0.f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int h = g + 8 * r;
+        if (h < GT) {
+          float* dst = mbuf + (warp * GT + h) * (D + 2);
+          // n-tile nt = 2*chunk + parity holds dims 16*chunk + 2*col + parity
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            const int d0 = 16 * (n >> 1) + 4 * tq + (n & 1);
+            dst[d0] = O[n][2 * r] * vup;
+            dst[d0 + 2] = O[n][2 * r + 1] * vup;
+          }
+          if (tq == 0) {
+            dst[D] = mr[r];
+            dst[D + 1] = lr[r];
+          }
+        }
+      }
+    } else if constexpr (MMA) {
       // Query heads h0..h0+GT-1 are the M rows of m16n8k16 (rows >= GT are
       // zero); K rows are the N columns of S = Q K^T, and P (bf16) times V
       // accumulates O[16 x D] in registers.  Lane (g = lane/4, tq = lane%4)
@@ -778,8 +1033,8 @@ struct Launch {
   const void* merge;
 };
 
-// e4m3-pool instances (pa_decode_fp8.cu): bf16 queries, CUDA-core path,
-// hg KV heads per work item.
-Launch pick_decode_fp8(int head_dim, int gt, int hg);
+// e4m3-pool instances (pa_decode_fp8.cu): bf16 queries, hg KV heads per
+// work item, tensor cores (head_dim 128, gt a power of two >= 2) or CUDA cores.
+Launch pick_decode_fp8(int head_dim, int gt, int hg, bool mma);
 
 }  // namespace pa

@@ -140,7 +140,8 @@ def test_decode_fp8_matches_oracle(pa, name, partition):
 
 @pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 8, 128, 16), (16, 4, 64, 8), (32, 8, 64, 32), (8, 2, 128, 8),
                                          (16, 8, 128, 32), (12, 4, 128, 16), (8, 4, 32, 16), (8, 2, 128, 4),
-                                         (64, 8, 128, 16), (6, 2, 64, 16)])
+                                         (64, 8, 128, 16), (6, 2, 64, 16), (32, 2, 128, 16), (64, 2, 128, 16),
+                                         (8, 1, 128, 16)])
 def test_decode_fp8_shape_variants(pa, Hq, Hkv, D, bs):
     c = _case("c4", B=3, Hq=Hq, Hkv=Hkv, D=D, bs=bs, len_dist=("uniform", 1, 1500))
     ref = oracle_fp8(c)
