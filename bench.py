@@ -48,6 +48,9 @@ WORKLOAD_TEXT = {
             "other scattered device blocks",
     "c5prefill": "bf16 GQA 32/8 causal chunked-prefill tile: 64 prompts, 512 queries at positions 512..1023 "
                  "over a 1024-token paged context (block_size 16), tensor cores",
+    "mixed": "one mixed round in one launch (pa_prefill_varlen): 8 prompts each running a 512-token prefill "
+             "chunk at the end of a 1024-token context + 256 decode requests over contexts U[128,2048]; "
+             "bf16 GQA 32/8, head_dim 128, block_size 16",
     "c5": "bf16 GQA decode 32/8, 64 prompts x 8 samples sharing 1024-token prompts + private tails U[0,256]; "
           "plus reshape_and_cache of the new tokens",
 }
@@ -350,6 +353,38 @@ def run_reference_swap(args):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_mixed(args):
+    """Oracle mixed round on one host core: each step is a slice of the
+    mixed workload (one prefill prompt's last 8 query rows + 4 decode
+    requests)."""
+    import numpy as np
+    import torch
+    import oracle
+    from paged_kv_cache_307_gb300 import workloads as W
+    c = W.mixed_case(device="cpu", n_prefill=1, n_decode=4, chunk=8, nan_fill=False)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    k, v, q = f64(c["k_cache"]), f64(c["v_cache"]), f64(c["q"])
+    qs, lens, tables = c["query_start"].numpy(), c["context_lens"].numpy(), c["block_tables"].numpy()
+    flops = W.varlen_flops(lens, np.diff(qs), q.shape[1], q.shape[2])
+    for _ in range(args.warmup):
+        oracle.paged_prefill_varlen(q, qs, k, v, tables, lens, c["scale"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_prefill_varlen(q, qs, k, v, tables, lens, c["scale"])
+    dt = time.perf_counter() - t0
+    val = flops * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": "mixed round attention TFLOP/s (bf16, unmasked work)",
+            "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "mixed: " + WORKLOAD_TEXT["mixed"],
+                       "sample": "one 8-row prefill slice + 4 decode requests per step"},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d steps of one 8-row prefill slice + 4 decode requests" % args.steps},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle timed on one host core: each step is one (sequence, KV head)
     slice of the workload (append + decode), cycling through a 16-sequence
@@ -360,6 +395,8 @@ def run_reference(args, rank, world):
         return run_reference_prefill(args)
     if args.workload == "swap":
         return run_reference_swap(args)
+    if args.workload == "mixed":
+        return run_reference_mixed(args)
     fp8 = args.workload.endswith("fp8")
     tasks, nbytes = (_cpu_tasks_fp8 if fp8 else _cpu_tasks)(args.workload, 16, seed=12345)
     fn = _oracle_seq_fp8 if fp8 else _oracle_slice
@@ -597,6 +634,112 @@ def run_swap(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_mixed(args, rank, world, local_rank):
+    """One mixed round (decode requests + prefill chunks) through
+    pa_prefill_varlen.  Metric: TFLOP/s of the unmasked causal work.  The
+    same round as two calls (the chunks through pa_prefill_paged, the decode
+    requests through pa_decode) is timed beside it."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_307_gb300 import build as B
+    B.build()
+    from paged_kv_cache_307_gb300 import _lib as pa
+    from paged_kv_cache_307_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    case = W.mixed_case(device=dev, seed=W.SPECS["c5"].seed + 1000 * rank, nan_fill=False)
+    q = case["q"]
+    rows, Hq, D = q.shape
+    out = torch.empty_like(q)
+    lens = case["context_lens"].cpu().numpy()
+    qs = case["query_start"].cpu().numpy()
+    nq = np.diff(qs)
+    flops = W.varlen_flops(lens, nq, Hq, D)
+    npf, ndec = case["n_prefill"], case["n_decode"]
+    Hkv = case["k_cache"].shape[2]
+    kv_bytes = int(lens.sum()) * 2 * Hkv * D * 2
+    stream = torch.cuda.current_stream()
+
+    def step(qq=q):
+        pa.prefill_varlen(out, qq, case["query_start"], case["k_cache"], case["v_cache"], case["block_tables"],
+                          case["context_lens"], case["scale"])
+
+    # the same round as two calls
+    chunk = int(nq[0]) if npf else 0
+    q_pf = q[:npf * chunk].reshape(npf, chunk, Hq, D) if npf else None
+    out_pf = torch.empty_like(q_pf) if npf else None
+    q_dec = q[npf * chunk:].contiguous()
+    out_dec = torch.empty_like(q_dec)
+    tab_pf, tab_dec = case["block_tables"][:npf].contiguous(), case["block_tables"][npf:].contiguous()
+    len_pf, len_dec = case["context_lens"][:npf].contiguous(), case["context_lens"][npf:].contiguous()
+    ws = pa.alloc_workspace(q_dec, case["k_cache"], tab_dec)
+
+    def split_step():
+        if npf:
+            pa.prefill(out_pf, q_pf, case["k_cache"], case["v_cache"], tab_pf, len_pf, case["scale"])
+        pa.decode(out_dec, q_dec, case["k_cache"], case["v_cache"], tab_dec, len_dec, case["scale"], workspace=ws)
+
+    def timed(fn, K):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+
+    K = min(args.steps, 500)
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    sampler = ClockSampler(int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].isdigit()
+                           else local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    ms = timed(step, K)
+    clocks = sampler.stop()
+    assert pa.last_error() == 0
+    split_ms = timed(split_step, K)
+    assert pa.last_error() == 0
+    qh = q.cpu().pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd = torch.empty_like(q)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        step(qq=qd)
+        oh.copy_(out, non_blocking=True)
+
+    e2e_ms = timed(e2e_step, min(K, 100))
+    if rank != 0:
+        return
+    peak, src = tensor_peak()
+    tflops = world * flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "mixed round attention TFLOP/s (bf16, unmasked work)", "value": round(tflops, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "mixed: " + WORKLOAD_TEXT["mixed"], "prefill_chunks": int(npf),
+                   "decode_requests": int(ndec), "query_rows": int(rows), "flops_per_step": flops,
+                   "kv_bytes_per_step": kv_bytes, "l2": "K/V pool larger than L2; no flush"},
+        "kv_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 2),
+        "tokens_per_s": round(world * rows / (ms / 1e3), 1),
+        "split_calls": {"ms_per_step": round(split_ms, 5),
+                        "note": "the same round as pa_prefill_paged (chunks) + pa_decode (decode requests)"},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4), "traffic": None,
+                     "kernel": "prefill_kernel over ragged query counts (tcgen05.mma, TMEM accumulators)",
+                     "peak_source": "%s bf16 (MEASURED_PEAKS.json)" % src},
+        "e2e": {"value": round(world * flops / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": qh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -809,6 +952,8 @@ def main():
             run_prefill(args, rank, world, local_rank)
         elif args.workload == "swap":
             run_swap(args, rank, world, local_rank)
+        elif args.workload == "mixed":
+            run_mixed(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -305,6 +305,35 @@ int pa_prefill_paged(void* out, const void* query, int num_queries,
                      int block_size, int num_blocks, float scale,
                      pa_dtype dtype, void* stream);
 
+/*
+ * Mixed round in one launch: decode requests and prefill chunks together
+ * ([OS] §8.1 chunked prefill; §8.2: one round's token budget covers decode
+ * tokens, new prefill tokens and chunked-prefill tokens).  Sequence b
+ * contributes n_b = query_start[b+1] - query_start[b] query rows, its last
+ * n_b tokens (K/V already appended): n_b = 1 for a decode request, the chunk
+ * length for a prefill chunk, 0 for a sequence with no work this round.
+ * Row i of sequence b sits at position p = context_lens[b] - n_b + i and
+ * attends causally to positions 0..p (rows with p < 0 are zeros).
+ *
+ *   out, query     [total_queries, num_heads, head_dim], rows in sequence
+ *                  order: sequence b's rows start at query_start[b]
+ *   query_start    [num_seqs + 1] int32, device, non-decreasing, starting
+ *                  at 0 and ending at total_queries (a decreasing pair sets
+ *                  PA_DEV_BAD_LEN and that sequence writes nothing)
+ *   other arguments as for pa_prefill_paged; num_seqs <= 2048
+ *
+ * The same tcgen05 kernel as pa_prefill_paged: each (query tile, KV head)
+ * is one CTA, tiles of 128 / G query positions; a decode request is a
+ * tile with one position.
+ */
+int pa_prefill_varlen(void* out, const void* query, const int32_t* query_start, int total_queries,
+                      const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs,
+                      int num_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, float scale,
+                      pa_dtype dtype, void* stream);
+
 /* Return the sticky device-detected condition bits (PA_DEV_*) and clear
  * them.  Synchronises the current device; 0 means nothing was detected.
  * Returns PA_ERR_CUDA if the device cannot be read. */

@@ -40,6 +40,7 @@ from .attention import (  # noqa: F401
     merge_partials,
     paged_decode_split,
     paged_prefill,
+    paged_prefill_varlen,
 )
 from .cache_ops import reshape_and_cache, copy_blocks, swap_blocks  # noqa: F401
 from .quant import (  # noqa: F401

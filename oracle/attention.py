@@ -248,3 +248,24 @@ def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, scale):
                 continue
             out[b, i] = dense_attention(q[b, i], K[:pos + 1], V[:pos + 1], scale)
     return out
+
+
+def paged_prefill_varlen(q, query_start, k_cache, v_cache, block_tables, context_lens, scale):
+    """Attention for a mixed round: sequence b contributes the query rows
+    q[query_start[b]:query_start[b+1]] ([rows, Hq, D]), its last
+    n_b = query_start[b+1] - query_start[b] tokens, their K/V already in the
+    pool.  [OS] §8.1–8.2: one round holds decode tokens (n_b = 1) and prefill
+    chunk tokens under one token budget; a chunk continues from the tokens
+    already computed.  Each row attends causally to its paged context, as in
+    ``paged_prefill``.  Returns [rows, Hq, D] f64; rows at negative
+    positions are zero."""
+    q = _as_f64(q)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in range(len(context_lens)):
+        s0, s1 = int(query_start[b]), int(query_start[b + 1])
+        if s1 <= s0:
+            continue
+        out[s0:s1] = paged_prefill(q[s0:s1][None], k_cache, v_cache, block_tables[b:b + 1],
+                                   context_lens[b:b + 1], scale)[0]
+    return out
+

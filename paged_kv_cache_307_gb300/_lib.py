@@ -46,6 +46,8 @@ lib.pa_reshape_and_cache_fp8.restype = _i
 lib.pa_decode_fp8.argtypes = [_p, _p, _p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz,
                               _i, _p]
 lib.pa_decode_fp8.restype = _i
+lib.pa_prefill_varlen.argtypes = [_p, _p, _i32p, _i, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
+lib.pa_prefill_varlen.restype = _i
 lib.pa_swap_blocks.argtypes = [_p, _p, _i, _p, _p, _i, _i64p, _i, _i, _i, _i, _i, _p]
 lib.pa_swap_blocks.restype = _i
 lib.pa_last_error.argtypes = []
@@ -201,6 +203,20 @@ def prefill(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=
     _check(lib.pa_prefill_paged(_ptr(out), _ptr(q), Tq, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                 block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
                                 ctypes.c_float(scale), _dtype(q), _stream(stream)), "pa_prefill_paged")
+    return out
+
+
+def prefill_varlen(out, q, query_start, k_cache, v_cache, block_tables, context_lens, scale, stream=None):
+    """Mixed round: q/out [rows, Hq, D], sequence b's rows are
+    query_start[b]..query_start[b+1]-1, the last tokens of its context."""
+    _contig(out, q, query_start, k_cache, v_cache, block_tables, context_lens)
+    assert query_start.dtype == torch.int32 and block_tables.dtype == torch.int32
+    rows, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = context_lens.shape[0]
+    _check(lib.pa_prefill_varlen(_ptr(out), _ptr(q), _ptr(query_start), rows, _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs,
+                                 NB, ctypes.c_float(scale), _dtype(q), _stream(stream)), "pa_prefill_varlen")
     return out
 
 

@@ -58,7 +58,8 @@ constexpr uint32_t kOffQ = 0;          // Q: 2 halves x 16 KB
 constexpr uint32_t kOffK = 32768;      // K: 2 stages x (2 halves x 8 KB)
 constexpr uint32_t kOffV = 65536;      // V: 2 stages x (2 halves x 8 KB)
 constexpr uint32_t kOffBar = 98304;
-constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;   // + barriers + alignment slack
+constexpr uint32_t kOffTab = kOffBar + 128;  // ragged batches: tile prefix [B+1] + 8 warp sums
+constexpr uint32_t kSmemBytes = kOffTab + 1024;          // + alignment slack (fixed query count)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 // TMEM columns: S buffers at 0 and 64 (fp32, 64 keys each; P overwrites the
@@ -70,10 +71,15 @@ struct PrefillParams {
   void* out;
   const int32_t* block_tables;
   const int32_t* context_lens;
+  const int32_t* query_start;   // ragged batch: [B+1] cumulative query counts; null: Tq each
   int B, Tq, Hq, Hkv, G, QP, n_qt;
   int max_blocks, bs, num_blocks;
   float qscale;
 };
+
+// Ragged batches up to this many sequences: each CTA keeps the prefix of
+// query tiles per sequence in shared memory (4 bytes per sequence).
+constexpr int kVarlenMaxSeqs = 2048;
 
 // Key tile j uses K/V stage j & 1 and S/P buffer j & 1; each has its own
 // barriers.  tcgen05 operations from the MMA thread execute in issue order
@@ -115,11 +121,65 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
   const int lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------------- work item
-  const int per = p.B * p.Hkv;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x / per);      // longest tiles first
-  const int rem = (int)(blockIdx.x % per);
-  const int b = rem / p.Hkv;
-  const int kvh = rem % p.Hkv;
+  // Fixed count: (query tile, sequence, KV head) with the longest tiles of
+  // every sequence first.  Ragged batch (query_start given): the tiles of all
+  // sequences numbered sequence by sequence through a prefix table built by
+  // every CTA; CTAs past the last tile have nothing to do.
+  int b, kvh, qt, nq, qrow0;
+  if (p.query_start == nullptr) {
+    const int per = p.B * p.Hkv;
+    qt = p.n_qt - 1 - (int)(blockIdx.x / per);
+    const int rem = (int)(blockIdx.x % per);
+    b = rem / p.Hkv;
+    kvh = rem % p.Hkv;
+    nq = p.Tq;
+    qrow0 = b * p.Tq;
+  } else {
+    int* tpre = reinterpret_cast<int*>(smem + kOffTab);         // [B+1] tile prefix
+    int* wsum = tpre + p.B + 1;
+    const int per = (p.B + kThreads - 1) / kThreads;
+    const int b0 = min(p.B, (int)threadIdx.x * per), b1 = min(p.B, b0 + per);
+    int sum = 0;
+    for (int i = b0; i < b1; ++i) {
+      const int n = __ldg(&p.query_start[i + 1]) - __ldg(&p.query_start[i]);
+      sum += n > 0 ? (n + p.QP - 1) / p.QP : 0;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int i = b0; i < b1; ++i) {
+      tpre[i] = run;
+      const int n = __ldg(&p.query_start[i + 1]) - __ldg(&p.query_start[i]);
+      run += n > 0 ? (n + p.QP - 1) / p.QP : 0;
+    }
+    if (threadIdx.x == kThreads - 1) tpre[p.B] = run;
+    __syncthreads();
+    const int t = (int)(blockIdx.x / p.Hkv);
+    kvh = (int)(blockIdx.x % p.Hkv);
+    if (t >= tpre[p.B]) return;                     // no tile: nothing allocated yet
+    int lo = 0, hi = p.B - 1;                       // the sequence holding tile t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tpre[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    b = lo;
+    const int ntb = tpre[b + 1] - tpre[b];
+    qt = ntb - 1 - (t - tpre[b]);                   // the sequence's longest tile first
+    qrow0 = __ldg(&p.query_start[b]);
+    nq = __ldg(&p.query_start[b + 1]) - qrow0;
+    if (nq < 0) {                                   // decreasing starts: flagged, nothing written
+      if (threadIdx.x == 0) atomicOr(&g_status_prefill, PA_DEV_BAD_LEN);
+      return;
+    }
+  }
   const int q0 = qt * p.QP;
   int L = __ldg(&p.context_lens[b]);
   const int Lmax = p.max_blocks * p.bs;
@@ -127,7 +187,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     if (threadIdx.x == 0 && qt == p.n_qt - 1 && kvh == 0) atomicOr(&g_status_prefill, PA_DEV_BAD_LEN);
     L = L < 0 ? 0 : Lmax;
   }
-  const int pos0 = L - p.Tq + q0;                 // position of the tile's first query
+  const int pos0 = L - nq + q0;                   // position of the tile's first query
   const int kend = min(L, pos0 + p.QP);           // keys this tile needs: [0, kend)
   const int nt = kend > 0 ? (kend + kKT - 1) / kKT : 0;
 
@@ -165,8 +225,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         prefetch_tensormap(&mapV);
         mbar_arrive_expect_tx(&bars->q, 2 * kQHalf);
         const uint64_t pol = policy_evict_first();
-        tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, q0, b, pol);
-        tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, q0, b, pol);
+        // Q as [rows, Hq, D]: rows past the sequence's queries (a ragged
+        // tile) belong to the next sequence or are zero-filled past the end;
+        // their scores are computed and never written.
+        tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, qrow0 + q0, 0, pol);
+        tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, qrow0 + q0, 0, pol);
       }
       issued_q = 1;
       const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by other query tiles
@@ -268,7 +331,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     const int r = quarter * 32 + lane;            // tile row
     const int qi = r / p.G, hh = r % p.G;
     const int pos = pos0 + qi;
-    const bool row_out = (q0 + qi) < p.Tq;
+    const bool row_out = (q0 + qi) < nq;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     float m_ref = -INFINITY, lsum = 0.f;
     bool live = true;
@@ -374,7 +437,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     unsigned char* orow = static_cast<unsigned char*>(p.out) +
-                          (((size_t)b * p.Tq + q0 + qi) * p.Hq + (size_t)kvh * p.G + hh) * (kD * 2);
+                          (((size_t)qrow0 + q0 + qi) * p.Hq + (size_t)kvh * p.G + hh) * (kD * 2);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
@@ -418,28 +481,32 @@ unsigned fetch_status_prefill() {
 
 using namespace pa;
 
-extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, const void* k_cache,
-                                const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
-                                const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
-                                int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
-                                void* stream) {
+// Shared by pa_prefill_paged (query_start null: num_queries per sequence)
+// and pa_prefill_varlen (query_start [B+1]; rows = total query rows).
+static int prefill_impl(void* out, const void* query, const int32_t* query_start, int num_queries, int rows,
+                        const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                        pa_dtype dtype, void* stream) {
   if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
   if (dtype != PA_BF16 || head_dim != 128) return PA_ERR_SHAPE;
-  if (num_seqs < 0 || num_queries < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
-      num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+  if (num_seqs < 0 || num_queries < 0 || rows < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+      num_heads % num_kv_heads || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
       !(block_size == 8 || block_size == 16 || block_size == 32))
     return PA_ERR_SHAPE;
+  if (query_start && num_seqs > kVarlenMaxSeqs) return PA_ERR_SHAPE;
   const int G = num_heads / num_kv_heads;
   if (G > 16 || (128 % G) != 0 || !(scale > 0.f)) return PA_ERR_SHAPE;
-  if (num_seqs == 0 || num_queries == 0) return PA_OK;
+  if (num_seqs == 0 || rows == 0) return PA_OK;
   if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
 
   const int QP = 128 / G;
   CUtensorMap mapQ, mapK, mapV;
   {
-    const uint64_t dims[4] = {128, (uint64_t)num_heads, (uint64_t)num_queries, (uint64_t)num_seqs};
-    const uint64_t str[3] = {256, (uint64_t)num_heads * 256, (uint64_t)num_queries * num_heads * 256};
+    // queries as [rows, Hq, D] (one more unit dimension for the 4-D copy)
+    const uint64_t dims[4] = {128, (uint64_t)num_heads, (uint64_t)rows, 1};
+    const uint64_t str[3] = {256, (uint64_t)num_heads * 256, (uint64_t)rows * num_heads * 256};
     const uint32_t box[4] = {64, (uint32_t)G, (uint32_t)QP, 1};
     if (!encode_map(&mapQ, query, PA_BF16, 4, dims, str, box, true)) {
       note_host_error("cuTensorMapEncodeTiled failed for the query tile");
@@ -464,6 +531,7 @@ extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, c
   prm.out = out;
   prm.block_tables = block_tables;
   prm.context_lens = context_lens;
+  prm.query_start = query_start;
   prm.B = num_seqs;
   prm.Tq = num_queries;
   prm.Hq = num_heads;
@@ -475,11 +543,37 @@ extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, c
   prm.bs = block_size;
   prm.num_blocks = num_blocks;
   prm.qscale = scale * kLog2e;
-  const long long grid = (long long)prm.n_qt * num_seqs * num_kv_heads;
+  // ragged: at most ceil(rows/QP) + B query tiles in all
+  const long long tiles = query_start ? (long long)(rows + QP - 1) / QP + num_seqs
+                                      : (long long)prm.n_qt * num_seqs;
+  const long long grid = tiles * num_kv_heads;
+  const size_t smem = kSmemBytes + (query_start ? 4 * ((size_t)num_seqs + 1 + 8) : 0);
   void* args[] = {&mapQ, &mapK, &mapV, &prm};
   if (!ck(cudaLaunchKernel(reinterpret_cast<const void*>(&prefill_kernel), dim3((unsigned)grid), dim3(kThreads),
-                           args, kSmemBytes, (cudaStream_t)stream),
+                           args, smem, (cudaStream_t)stream),
           "cudaLaunchKernel(prefill_kernel)"))
     return PA_ERR_CUDA;
   return PA_OK;
+}
+
+extern "C" int pa_prefill_paged(void* out, const void* query, int num_queries, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                int head_dim, int block_size, int num_blocks, float scale, pa_dtype dtype,
+                                void* stream) {
+  if (num_seqs < 0 || num_queries < 0 || (long long)num_seqs * num_queries > 0x7fffffffll) return PA_ERR_SHAPE;
+  return prefill_impl(out, query, nullptr, num_queries, num_seqs * num_queries, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, scale, dtype, stream);
+}
+
+extern "C" int pa_prefill_varlen(void* out, const void* query, const int32_t* query_start, int total_queries,
+                                 const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                 int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_heads,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                                 pa_dtype dtype, void* stream) {
+  if (num_seqs > 0 && total_queries > 0 && !query_start) return PA_ERR_NULL;
+  return prefill_impl(out, query, query_start, 0, total_queries, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, scale, dtype, stream);
 }

@@ -334,6 +334,49 @@ def prefill_case(small=False, device="cpu", seed=None, prompts=None, Tq=512, pre
             "scale": scale_for(spec.D), "Tq": Tq, "block_size": bs}
 
 
+def mixed_case(small=False, device="cpu", seed=None, n_decode=None, n_prefill=None, chunk=512, prefix=1024,
+               decode_lens=("uniform", 128, 2048), nan_fill=True):
+    """One mixed round ([OS] §8.1–8.2): ``n_prefill`` prompts each running a
+    ``chunk``-token prefill chunk at the end of a ``prefix``-token context,
+    and ``n_decode`` requests each decoding one token over a context drawn
+    from ``decode_lens``; every query's K/V already in the pool.  Queries
+    are packed [rows, Hq, D] in sequence order (prefill chunks first) with
+    ``query_start`` [B+1].  c5 shapes (GQA 32/8, D 128, bs 16)."""
+    spec = SPECS["c5"]
+    seed = (spec.seed if seed is None else seed) + 300
+    rng = np.random.default_rng(seed)
+    n_prefill = (2 if small else 8) if n_prefill is None else n_prefill
+    n_decode = (6 if small else 256) if n_decode is None else n_decode
+    _, lo, hi = decode_lens
+    dl = rng.integers(lo, hi + 1, size=n_decode)
+    lens = np.concatenate([np.full(n_prefill, prefix, dtype=np.int64), dl.astype(np.int64)])
+    nq = np.concatenate([np.full(n_prefill, chunk, dtype=np.int64), np.ones(n_decode, dtype=np.int64)])
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    bs = spec.bs
+    tables, NB, _ = _tables(lens, bs, 0, spec.spare, rng)
+    dt = DTYPES[spec.dtype]
+    gen = _generator(device, seed)
+    k = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    v = _randn((NB, bs, spec.Hkv, spec.D), dt, gen, device)
+    q = _randn((int(qs[-1]), spec.Hq, spec.D), dt, gen, device)
+    tables_t = torch.from_numpy(tables)
+    _nan_unused(k, v, tables_t, lens, bs, nan_fill)
+    return {"q": q, "query_start": torch.from_numpy(qs).to(device), "k_cache": k, "v_cache": v,
+            "block_tables": tables_t.to(device), "context_lens": torch.from_numpy(lens.astype(np.int32)).to(device),
+            "scale": scale_for(spec.D), "block_size": bs, "n_prefill": n_prefill, "n_decode": n_decode}
+
+
+def varlen_flops(lens, nq, Hq, D):
+    """Unmasked multiply-add FLOPs of a mixed round: query i of n at position
+    L - n + i attends to L - n + i + 1 keys."""
+    tot = 0
+    for L, n in zip(lens, nq):
+        L, n = int(L), int(n)
+        for i in range(n):
+            tot += max(0, L - n + i + 1)
+    return 4 * Hq * D * tot
+
+
 def prefill_flops(lens, Tq, Hq, D):
     """Multiply-add FLOPs of the causal tile (QK^T and PV, 2 flops per MAC),
     counting only unmasked (query, key) pairs."""

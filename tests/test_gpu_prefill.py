@@ -99,3 +99,92 @@ def test_prefill_full_size_sampled(pa):
     got = f64(out)
     assert np.isfinite(got).all()
     assert_close(got[seqs], ref, "bf16")
+
+
+# ------------------------------------------------------------------ mixed rounds (ragged query counts)
+
+def _oracle_varlen(case, seqs=None):
+    lens = case["context_lens"].cpu().numpy()
+    tables = case["block_tables"].cpu().numpy()
+    qs = case["query_start"].cpu().numpy()
+    bs = case["block_size"]
+    seqs = list(range(len(lens))) if seqs is None else list(seqs)
+    used = sorted({int(tables[b, j]) for b in seqs for j in range(-(-int(lens[b]) // bs))})
+    index = {blk: i for i, blk in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=case["k_cache"].device)
+    k = f64(case["k_cache"].index_select(0, idx))
+    v = f64(case["v_cache"].index_select(0, idx))
+    nt = np.zeros((len(seqs), tables.shape[1]), dtype=np.int64)
+    for r, b in enumerate(seqs):
+        for j in range(-(-int(lens[b]) // bs)):
+            nt[r, j] = index[int(tables[b, j])]
+    rows = [np.arange(qs[b], qs[b + 1]) for b in seqs]
+    sub_qs = np.concatenate([[0], np.cumsum([len(r) for r in rows])])
+    q = f64(case["q"])[np.concatenate(rows)] if sub_qs[-1] else f64(case["q"])[:0]
+    return oracle.paged_prefill_varlen(q, sub_qs, k, v, nt, lens[seqs], case["scale"]), np.concatenate(rows)
+
+
+def _run_varlen(pa, case):
+    out = torch.full_like(case["q"], float("nan"))
+    pa.prefill_varlen(out, case["q"], case["query_start"], case["k_cache"], case["v_cache"],
+                      case["block_tables"], case["context_lens"], case["scale"])
+    torch.cuda.synchronize()
+    return out
+
+
+def test_mixed_round_small(pa):
+    case = W.mixed_case(small=True, device="cuda")
+    ref, rows = _oracle_varlen(case)
+    out = _run_varlen(pa, case)
+    assert pa.last_error() == 0
+    assert_close(f64(out)[rows], ref, "bf16")
+
+
+@pytest.mark.parametrize("chunk", [1, 31, 32, 33, 100])
+def test_mixed_round_ragged_chunks_and_empty_sequences(pa, chunk):
+    case = W.mixed_case(small=True, device="cuda", chunk=chunk, prefix=300, n_decode=5, n_prefill=3)
+    # give sequence 1 no work this round: drop its rows from the packing
+    qs = case["query_start"].cpu().numpy().astype(np.int64)
+    n = np.diff(qs)
+    keep = np.concatenate([np.arange(qs[b], qs[b + 1]) for b in range(len(n)) if b != 1])
+    n[1] = 0
+    case["q"] = case["q"][torch.from_numpy(keep).cuda()].contiguous()
+    case["query_start"] = torch.from_numpy(np.concatenate([[0], np.cumsum(n)]).astype(np.int32)).cuda()
+    ref, rows = _oracle_varlen(case)
+    out = _run_varlen(pa, case)
+    assert pa.last_error() == 0
+    assert_close(f64(out)[rows], ref, "bf16")
+
+
+def test_uniform_round_equals_fixed_count_tile(pa):
+    case = W.prefill_case(small=True, device="cuda", Tq=96)
+    fixed = _run(pa, case)
+    P, Tq, Hq, D = case["q"].shape
+    vl = dict(case, q=case["q"].reshape(P * Tq, Hq, D),
+              query_start=torch.arange(0, (P + 1) * Tq, Tq, dtype=torch.int32, device="cuda"))
+    out = _run_varlen(pa, vl)
+    assert pa.last_error() == 0
+    assert torch.equal(out.view(torch.int16), fixed.reshape(P * Tq, Hq, D).view(torch.int16))
+
+
+def test_decode_only_round_matches_decode_oracle(pa):
+    case = W.mixed_case(small=True, device="cuda", n_prefill=0, n_decode=12)
+    ref, rows = _oracle_varlen(case)
+    out = _run_varlen(pa, case)
+    assert pa.last_error() == 0
+    assert_close(f64(out)[rows], ref, "bf16")
+
+
+def test_mixed_round_full_size_sampled(pa):
+    case = W.mixed_case(device="cuda")
+    lens = case["context_lens"].cpu().numpy()
+    rng = np.random.default_rng(3)
+    seqs = sorted(set([0, int(case["n_prefill"]) - 1] +
+                      (case["n_prefill"] + rng.choice(case["n_decode"], 6, replace=False)).tolist()))
+    ref, rows = _oracle_varlen(case, seqs)
+    out = _run_varlen(pa, case)
+    assert pa.last_error() == 0
+    got = f64(out)
+    assert np.isfinite(got).all()
+    assert_close(got[rows], ref, "bf16")
+    assert len(lens) == case["n_prefill"] + case["n_decode"]

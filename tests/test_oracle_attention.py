@@ -355,3 +355,28 @@ def test_planted_mistakes_are_caught():
     assert not _pins_pass(walk=walk_no_rescale)
     assert not _pins_pass(walk=walk_reads_whole_block)
     assert not _pins_pass(merge=merge_unweighted)
+
+
+def test_varlen_round_reduces_to_decode_and_fixed_chunks():
+    """A mixed round: decode rows equal single-query decode; a uniform round
+    equals the fixed-count tile; empty sequences contribute no rows."""
+    rng = np.random.default_rng(17)
+    NB, bs, Hkv, G, D = 24, 4, 2, 2, 8
+    k = rng.standard_normal((NB, bs, Hkv, D))
+    v = rng.standard_normal((NB, bs, Hkv, D))
+    tables = rng.permutation(NB)[:18].reshape(3, 6)
+    lens = np.array([13, 7, 20])
+    n = np.array([1, 0, 5])                        # decode, empty, a 5-token chunk
+    qs = np.concatenate([[0], np.cumsum(n)])
+    q = rng.standard_normal((int(qs[-1]), Hkv * G, D))
+    out = oracle.paged_prefill_varlen(q, qs, k, v, tables, lens, 0.3)
+    dec = oracle.paged_decode(q[0:1], k, v, tables[0:1], lens[0:1], 0.3)
+    assert np.abs(out[0] - dec[0]).max() <= 1e-12
+    chunk = oracle.paged_prefill(q[1:6][None], k, v, tables[2:3], lens[2:3], 0.3)[0]
+    assert np.abs(out[1:6] - chunk).max() <= 1e-12
+    # a row's output depends only on its own query and its causal prefix
+    q2 = q.copy()
+    q2[3] += 1.0
+    out2 = oracle.paged_prefill_varlen(q2, qs, k, v, tables, lens, 0.3)
+    assert np.array_equal(np.delete(out2, 3, axis=0), np.delete(out, 3, axis=0))
+
