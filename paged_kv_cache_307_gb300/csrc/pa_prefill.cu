@@ -58,7 +58,7 @@ constexpr uint32_t kOffQ = 0;          // Q: 2 halves x 16 KB
 constexpr uint32_t kOffK = 32768;      // K: 2 stages x (2 halves x 8 KB)
 constexpr uint32_t kOffV = 65536;      // V: 2 stages x (2 halves x 8 KB)
 constexpr uint32_t kOffBar = 98304;
-constexpr uint32_t kOffTab = kOffBar + 128;  // ragged batches: tile prefix [B+1] + 8 warp sums
+constexpr uint32_t kOffTab = kOffBar + 256;  // ragged batches: tile prefix [B+1] + 8 warp sums
 constexpr uint32_t kSmemBytes = kOffTab + 1024;          // + alignment slack (fixed query count)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -87,10 +87,11 @@ constexpr int kVarlenMaxSeqs = 2048;
 // live in S buffer j & 1 until S_{j+2} (issued after P_j V_j) overwrites it,
 // and an S_j completion also proves that P_{j-2} V_{j-2} has completed.
 struct Bars {
-  uint64_t q, full_k[2], full_v[2], empty[2], s[2], p[2], pv[2], drain;
+  uint64_t q, full_k[2], full_v[2], empty_k[2], empty_v[2], s[2], p[2], pv[2], drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= kOffTab - kOffBar, "barrier block overlaps the tile table");
 
 // 2^x with the hardware approximation (flushes subnormal results to zero;
 // the products it feeds are rounded to bf16).
@@ -196,7 +197,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(&bars->full_k[s2], 1);
       mbar_init(&bars->full_v[s2], 1);
-      mbar_init(&bars->empty[s2], 1);
+      mbar_init(&bars->empty_k[s2], 1);
+      mbar_init(&bars->empty_v[s2], 1);
       mbar_init(&bars->s[s2], 1);
       mbar_init(&bars->p[s2], 128);
       mbar_init(&bars->pv[s2], 1);
@@ -217,7 +219,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    int issued_q = 0, issued = 0;
+    int issued_q = 0, issued_k = 0, issued_v = 0;
     if (nt > 0) {
       if (lane == 0) {
         prefetch_tensormap(&mapQ);
@@ -236,47 +238,64 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
       const int nbt = kKT / p.bs;
       const uint32_t rows_bytes = (uint32_t)p.bs * 128u;    // one half-box
-      for (int j = 0; j < nt; ++j) {
-        const int st = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1);
-        const int k0 = j * kKT;
-        const int nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
-        int blk = 0;
-        if (lane < nvalid) {
-          blk = __ldg(&row[k0 / p.bs + lane]);
-          if ((unsigned)blk >= (unsigned)p.num_blocks) {
-            atomicOr(&g_status_prefill, PA_DEV_BAD_BLOCK);
-            blk = 0;
+      // K of tile t can be reloaded as soon as S_{t-2} has completed, V only
+      // after P_{t-2} V_{t-2}; S_{t-2} completes first (the MMA thread issues
+      // S_{j+1} before P_j V_j), so K_t is loaded before V_{t-1}.
+      int blk_prev = 0, nvalid_prev = 0;
+      for (int t = 0; t <= nt; ++t) {
+        int blk = 0, nvalid = 0;
+        if (t < nt) {
+          const int st = t & 1;
+          const uint32_t u = (uint32_t)(t >> 1);
+          const int k0 = t * kKT;
+          nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
+          if (lane < nvalid) {
+            blk = __ldg(&row[k0 / p.bs + lane]);
+            if ((unsigned)blk >= (unsigned)p.num_blocks) {
+              atomicOr(&g_status_prefill, PA_DEV_BAD_BLOCK);
+              blk = 0;
+            }
           }
+          bool ok = true;
+          if (lane == 0) ok = wait_or_abort(&bars->empty_k[st], (u & 1u) ^ 1u, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bars->full_k[st], (uint32_t)nvalid * 2u * rows_bytes);
+          __syncwarp();
+          // lane jj loads block jj of the tile: one warp instruction per operand half
+          if (lane < nvalid) {
+            unsigned char* kdst = smem + kOffK + st * 2 * kKVHalf + lane * rows_bytes;
+            tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, blk, pol);
+            tma_load_4d(kdst + kKVHalf, &mapK, &bars->full_k[st], 64, kvh, 0, blk, pol);
+          }
+          issued_k = t + 1;
         }
-        bool ok = true;
-        if (lane == 0) ok = wait_or_abort(&bars->empty[st], (u & 1u) ^ 1u, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->full_k[st], (uint32_t)nvalid * 2u * rows_bytes);
-          mbar_arrive_expect_tx(&bars->full_v[st], (uint32_t)nvalid * 2u * rows_bytes);
+        if (t >= 1) {
+          const int tv = t - 1;
+          const int st = tv & 1;
+          const uint32_t u = (uint32_t)(tv >> 1);
+          bool ok = true;
+          if (lane == 0) ok = wait_or_abort(&bars->empty_v[st], (u & 1u) ^ 1u, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bars->full_v[st], (uint32_t)nvalid_prev * 2u * rows_bytes);
+          __syncwarp();
+          if (lane < nvalid_prev) {
+            unsigned char* vdst = smem + kOffV + st * 2 * kKVHalf + lane * rows_bytes;
+            tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, blk_prev, pol);
+            tma_load_4d(vdst + kKVHalf, &mapV, &bars->full_v[st], 64, kvh, 0, blk_prev, pol);
+          }
+          issued_v = tv + 1;
         }
-        __syncwarp();
-        // lane jj loads block jj of the tile: one warp instruction per operand half
-        if (lane < nvalid) {
-          unsigned char* kdst = smem + kOffK + st * 2 * kKVHalf + lane * rows_bytes;
-          unsigned char* vdst = smem + kOffV + st * 2 * kKVHalf + lane * rows_bytes;
-          tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, blk, pol);
-          tma_load_4d(kdst + kKVHalf, &mapK, &bars->full_k[st], 64, kvh, 0, blk, pol);
-          tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, blk, pol);
-          tma_load_4d(vdst + kKVHalf, &mapV, &bars->full_v[st], 64, kvh, 0, blk, pol);
-        }
-        issued = j + 1;
+        blk_prev = blk;
+        nvalid_prev = nvalid;
       }
     }
     // drain: no TMA write may land after the CTA exits
     if (lane == 0) {
       if (issued_q) mbar_wait(&bars->q, 0);
-      for (int j = max(0, issued - 2); j < issued; ++j) {
-        mbar_wait(&bars->full_k[j & 1], (uint32_t)(j >> 1) & 1u);
-        mbar_wait(&bars->full_v[j & 1], (uint32_t)(j >> 1) & 1u);
-      }
+      for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait(&bars->full_k[j & 1], (uint32_t)(j >> 1) & 1u);
+      for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait(&bars->full_v[j & 1], (uint32_t)(j >> 1) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -295,6 +314,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
                     kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s[j & 1]);
+        umma_commit(&bars->empty_k[j & 1]);    // K_j's stage is free once S_j is done
       };
       if (wait_or_abort(&bars->q, 0, abort_flag) && wait_or_abort(&bars->full_k[0], 0, abort_flag)) {
         tc_fence_after();
@@ -318,7 +338,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
                          (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&bars->pv[st]);
-          umma_commit(&bars->empty[st]);
+          umma_commit(&bars->empty_v[st]);
         }
       }
       // drain: every MMA issued so far has completed before TMEM is freed
