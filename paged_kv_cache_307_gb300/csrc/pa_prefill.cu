@@ -48,7 +48,7 @@ namespace {
 
 __device__ unsigned g_status_prefill;
 
-constexpr int kThreads = 192;          // 6 warps
+constexpr int kThreads = 224;          // 7 warps: K loads, MMA, 4 softmax, V loads
 constexpr int kRows = 128;             // query rows per tile
 constexpr int kKT = 64;                // keys per tile
 constexpr int kD = 128;
@@ -218,85 +218,70 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
   const uint32_t tmem = bars->tmem_base;
   const uint32_t tO = tmem + kColO;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    int issued_q = 0, issued_k = 0, issued_v = 0;
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 0 loads Q once and then K; warp 6 loads V.  K of tile t can be
+    // reloaded once S_{t-2} has completed, V only after P_{t-2} V_{t-2}: with
+    // one producer per operand neither waits behind the other's stage.
+    const bool is_k = warp == 0;
+    int issued_q = 0, issued = 0;
     if (nt > 0) {
       if (lane == 0) {
-        prefetch_tensormap(&mapQ);
-        prefetch_tensormap(&mapK);
-        prefetch_tensormap(&mapV);
-        mbar_arrive_expect_tx(&bars->q, 2 * kQHalf);
-        const uint64_t pol = policy_evict_first();
-        // Q as [rows, Hq, D]: rows past the sequence's queries (a ragged
-        // tile) belong to the next sequence or are zero-filled past the end;
-        // their scores are computed and never written.
-        tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, qrow0 + q0, 0, pol);
-        tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, qrow0 + q0, 0, pol);
+        if (is_k) {
+          prefetch_tensormap(&mapQ);
+          prefetch_tensormap(&mapK);
+          mbar_arrive_expect_tx(&bars->q, 2 * kQHalf);
+          const uint64_t pol = policy_evict_first();
+          // Q as [rows, Hq, D]: rows past the sequence's queries (a ragged
+          // tile) belong to the next sequence or are zero-filled past the
+          // end; their scores are computed and never written.
+          tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, qrow0 + q0, 0, pol);
+          tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, qrow0 + q0, 0, pol);
+        } else {
+          prefetch_tensormap(&mapV);
+        }
       }
-      issued_q = 1;
+      issued_q = is_k ? 1 : 0;
       const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by other query tiles
       const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
       const int nbt = kKT / p.bs;
       const uint32_t rows_bytes = (uint32_t)p.bs * 128u;    // one half-box
-      // K of tile t can be reloaded as soon as S_{t-2} has completed, V only
-      // after P_{t-2} V_{t-2}; S_{t-2} completes first (the MMA thread issues
-      // S_{j+1} before P_j V_j), so K_t is loaded before V_{t-1}.
-      int blk_prev = 0, nvalid_prev = 0;
-      for (int t = 0; t <= nt; ++t) {
-        int blk = 0, nvalid = 0;
-        if (t < nt) {
-          const int st = t & 1;
-          const uint32_t u = (uint32_t)(t >> 1);
-          const int k0 = t * kKT;
-          nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
-          if (lane < nvalid) {
-            blk = __ldg(&row[k0 / p.bs + lane]);
-            if ((unsigned)blk >= (unsigned)p.num_blocks) {
-              atomicOr(&g_status_prefill, PA_DEV_BAD_BLOCK);
-              blk = 0;
-            }
+      uint64_t* full = is_k ? bars->full_k : bars->full_v;
+      uint64_t* empty = is_k ? bars->empty_k : bars->empty_v;
+      const CUtensorMap* map = is_k ? &mapK : &mapV;
+      unsigned char* base = smem + (is_k ? kOffK : kOffV);
+      for (int t = 0; t < nt; ++t) {
+        const int st = t & 1;
+        const uint32_t u = (uint32_t)(t >> 1);
+        const int k0 = t * kKT;
+        const int nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
+        int blk = 0;
+        if (lane < nvalid) {
+          blk = __ldg(&row[k0 / p.bs + lane]);
+          if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            if (is_k) atomicOr(&g_status_prefill, PA_DEV_BAD_BLOCK);
+            blk = 0;
           }
-          bool ok = true;
-          if (lane == 0) ok = wait_or_abort(&bars->empty_k[st], (u & 1u) ^ 1u, abort_flag);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&bars->full_k[st], (uint32_t)nvalid * 2u * rows_bytes);
-          __syncwarp();
-          // lane jj loads block jj of the tile: one warp instruction per operand half
-          if (lane < nvalid) {
-            unsigned char* kdst = smem + kOffK + st * 2 * kKVHalf + lane * rows_bytes;
-            tma_load_4d(kdst, &mapK, &bars->full_k[st], 0, kvh, 0, blk, pol);
-            tma_load_4d(kdst + kKVHalf, &mapK, &bars->full_k[st], 64, kvh, 0, blk, pol);
-          }
-          issued_k = t + 1;
         }
-        if (t >= 1) {
-          const int tv = t - 1;
-          const int st = tv & 1;
-          const uint32_t u = (uint32_t)(tv >> 1);
-          bool ok = true;
-          if (lane == 0) ok = wait_or_abort(&bars->empty_v[st], (u & 1u) ^ 1u, abort_flag);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&bars->full_v[st], (uint32_t)nvalid_prev * 2u * rows_bytes);
-          __syncwarp();
-          if (lane < nvalid_prev) {
-            unsigned char* vdst = smem + kOffV + st * 2 * kKVHalf + lane * rows_bytes;
-            tma_load_4d(vdst, &mapV, &bars->full_v[st], 0, kvh, 0, blk_prev, pol);
-            tma_load_4d(vdst + kKVHalf, &mapV, &bars->full_v[st], 64, kvh, 0, blk_prev, pol);
-          }
-          issued_v = tv + 1;
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(&empty[st], (u & 1u) ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * rows_bytes);
+        __syncwarp();
+        // lane jj loads block jj of the tile: one warp instruction per operand half
+        if (lane < nvalid) {
+          unsigned char* dst = base + st * 2 * kKVHalf + lane * rows_bytes;
+          tma_load_4d(dst, map, &full[st], 0, kvh, 0, blk, pol);
+          tma_load_4d(dst + kKVHalf, map, &full[st], 64, kvh, 0, blk, pol);
         }
-        blk_prev = blk;
-        nvalid_prev = nvalid;
+        issued = t + 1;
       }
     }
     // drain: no TMA write may land after the CTA exits
     if (lane == 0) {
       if (issued_q) mbar_wait(&bars->q, 0);
-      for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait(&bars->full_k[j & 1], (uint32_t)(j >> 1) & 1u);
-      for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait(&bars->full_v[j & 1], (uint32_t)(j >> 1) & 1u);
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&(is_k ? bars->full_k : bars->full_v)[j & 1], (uint32_t)(j >> 1) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -364,30 +349,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       bool ok = wait_or_abort(&bars->s[st], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
       tc_fence_after();
-      float s[kKT];
+      // Pass 1: the row maximum of the raw scores (the causal mask only
+      // bites on tiles reaching past this row).  The scores are read again
+      // from TMEM in pass 2, which keeps fewer values live at once.
+      // Eight independent partial maxima keep the dependency chains short.
+      const bool full_tile = k0 + kKT - 1 <= pos;
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
       {
         uint32_t v[2][32];
         tmem_ld32(tmem + st * kKT + lane_off, v[0]);
         tmem_ld32(tmem + st * kKT + 32 + lane_off, v[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
-      }
-      // raw scores; the causal mask only bites on tiles reaching past this row.
-      // Eight independent partial maxima keep the dependency chains short.
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-      if (k0 + kKT - 1 <= pos) {
-#pragma unroll
-        for (int c = 0; c < kKT; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-      } else {
-#pragma unroll
         for (int c = 0; c < kKT; ++c) {
-          s[c] = (k0 + c <= pos) ? s[c] : -INFINITY;
-          mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+          const float x = __uint_as_float(v[c >> 5][c & 31]);
+          mx8[c & 7] = fmaxf(mx8[c & 7], (full_tile || k0 + c <= pos) ? x : -INFINITY);
         }
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -427,23 +405,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
           fence_proxy_async_smem();
         }
       }
-      // P = exp2(scale*s - m_ref) as bf16 pairs, written over this S buffer
+      // Pass 2: P = exp2(scale*s - m_ref) as bf16 pairs, written over this S
+      // buffer 32 keys at a time (packed column 16h + c holds keys 32h + 2c,
+      // 32h + 2c + 1; half 1's stores land on columns half 0 already read).
       const float negm = m_ref == -INFINITY ? 0.f : -m_ref;   // all-masked rows: every s is -inf
-      uint32_t pw[32];
       float ls8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], p.qscale, negm));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.qscale, negm));
-        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-        ls8[(2 * c) & 7] += __low2float(pk);
-        ls8[(2 * c + 1) & 7] += __high2float(pk);
-        pw[c] = *reinterpret_cast<const uint32_t*>(&pk);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tmem_ld32(tmem + st * kKT + hf * 32 + lane_off, v);
+        tmem_ld_wait();
+        uint32_t pw[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int kc = k0 + hf * 32 + 2 * c;
+          const float s0 = (full_tile || kc <= pos) ? __uint_as_float(v[2 * c]) : -INFINITY;
+          const float s1 = (full_tile || kc + 1 <= pos) ? __uint_as_float(v[2 * c + 1]) : -INFINITY;
+          const float p0 = ex2_approx(fmaf(s0, p.qscale, negm));
+          const float p1 = ex2_approx(fmaf(s1, p.qscale, negm));
+          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+          ls8[(2 * c) & 7] += __low2float(pk);
+          ls8[(2 * c + 1) & 7] += __high2float(pk);
+          pw[c] = *reinterpret_cast<const uint32_t*>(&pk);
+        }
+        tmem_st16(tmem + st * kKT + hf * 16 + lane_off, pw);
       }
       lsum += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      tmem_st32(tmem + st * kKT + lane_off, pw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p[st]);
