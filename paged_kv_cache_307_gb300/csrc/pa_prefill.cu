@@ -101,6 +101,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x for two f16 values at once (one MUFU operation for the pair).  P is
+// rounded to bf16 for the P V product, so the f16 result (11 significant
+// bits; inputs below -24 give 0) loses nothing that product keeps.
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (*abort_flag) return false;
   if (mbar_wait(bar, parity)) return true;
@@ -362,10 +371,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         tmem_ld32(tmem + st * kKT + lane_off, v[0]);
         tmem_ld32(tmem + st * kKT + 32 + lane_off, v[1]);
         tmem_ld_wait();
+        if (full_tile) {
 #pragma unroll
-        for (int c = 0; c < kKT; ++c) {
-          const float x = __uint_as_float(v[c >> 5][c & 31]);
-          mx8[c & 7] = fmaxf(mx8[c & 7], (full_tile || k0 + c <= pos) ? x : -INFINITY);
+          for (int c = 0; c < kKT; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c >> 5][c & 31]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKT; ++c)
+            mx8[c & 7] = fmaxf(mx8[c & 7], k0 + c <= pos ? __uint_as_float(v[c >> 5][c & 31]) : -INFINITY);
         }
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -417,15 +429,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         uint32_t v[32];
         tmem_ld32(tmem + st * kKT + hf * 32 + lane_off, v);
         tmem_ld_wait();
+        if (!full_tile) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (k0 + hf * 32 + c > pos) v[c] = __float_as_uint(-INFINITY);
+        }
         uint32_t pw[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int kc = k0 + hf * 32 + 2 * c;
-          const float s0 = (full_tile || kc <= pos) ? __uint_as_float(v[2 * c]) : -INFINITY;
-          const float s1 = (full_tile || kc + 1 <= pos) ? __uint_as_float(v[2 * c + 1]) : -INFINITY;
-          const float p0 = ex2_approx(fmaf(s0, p.qscale, negm));
-          const float p1 = ex2_approx(fmaf(s1, p.qscale, negm));
-          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+          // exponents in fp32, 2^x as an f16 pair, then bf16 for the product
+          const __half2 xh = __floats2half2_rn(fmaf(__uint_as_float(v[2 * c]), p.qscale, negm),
+                                               fmaf(__uint_as_float(v[2 * c + 1]), p.qscale, negm));
+          const uint32_t eh = ex2_f16x2(*reinterpret_cast<const uint32_t*>(&xh));
+          const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&eh));
+          const __nv_bfloat162 pk = __floats2bfloat162_rn(pf.x, pf.y);
           ls8[(2 * c) & 7] += __low2float(pk);
           ls8[(2 * c + 1) & 7] += __high2float(pk);
           pw[c] = *reinterpret_cast<const uint32_t*>(&pk);
