@@ -93,14 +93,6 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= kOffTab - kOffBar, "barrier block overlaps the tile table");
 
-// 2^x with the hardware approximation (flushes subnormal results to zero;
-// the products it feeds are rounded to bf16).
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // 2^x for two f16 values at once (one MUFU operation for the pair).  P is
 // rounded to bf16 for the P V product, so the f16 result (11 significant
 // bits; inputs below -24 give 0) loses nothing that product keeps.
