@@ -350,28 +350,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       bool ok = wait_or_abort(&bars->s[st], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
       tc_fence_after();
-      // Pass 1: the row maximum of the raw scores (the causal mask only
-      // bites on tiles reaching past this row).  The scores are read again
-      // from TMEM in pass 2, which keeps fewer values live at once.
-      // Eight independent partial maxima keep the dependency chains short.
+      // The row's 64 raw scores (the causal mask only bites on tiles
+      // reaching past this row) and their maximum.  Eight independent
+      // partial maxima keep the dependency chains short.
       const bool full_tile = k0 + kKT - 1 <= pos;
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-      {
-        uint32_t v[2][32];
-        tmem_ld32(tmem + st * kKT + lane_off, v[0]);
-        tmem_ld32(tmem + st * kKT + 32 + lane_off, v[1]);
-        tmem_ld_wait();
-        if (full_tile) {
+      uint32_t v[2][32];
+      tmem_ld32(tmem + st * kKT + lane_off, v[0]);
+      tmem_ld32(tmem + st * kKT + 32 + lane_off, v[1]);
+      tmem_ld_wait();
+      if (!full_tile) {
 #pragma unroll
-          for (int c = 0; c < kKT; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c >> 5][c & 31]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < kKT; ++c)
-            mx8[c & 7] = fmaxf(mx8[c & 7], k0 + c <= pos ? __uint_as_float(v[c >> 5][c & 31]) : -INFINITY);
-        }
+        for (int c = 0; c < kKT; ++c)
+          if (k0 + c > pos) v[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
+#pragma unroll
+      for (int c = 0; c < kKT; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c >> 5][c & 31]));
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       mx *= p.qscale;                                     // scale > 0 (checked by the host)
@@ -383,14 +379,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         ok = wait_or_abort(&bars->pv[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + lane_off + c * 32, v);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {         // 16 columns at a time: the scores stay live
+          uint32_t w[16];
+          tmem_ld16(tO + lane_off + c * 16, w);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tO + lane_off + c * 32, v);
+          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+          tmem_st16(tO + lane_off + c * 16, w);
         }
         tmem_st_wait();
       }
@@ -409,34 +405,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
           fence_proxy_async_smem();
         }
       }
-      // Pass 2: P = exp2(scale*s - m_ref) as bf16 pairs, written over this S
-      // buffer 32 keys at a time (packed column 16h + c holds keys 32h + 2c,
-      // 32h + 2c + 1; half 1's stores land on columns half 0 already read).
+      // P = exp2(scale*s - m_ref) as bf16 pairs, written over this S buffer
+      // 32 keys at a time (packed column 16h + c holds keys 32h + 2c,
+      // 32h + 2c + 1).  The row sum adds the f16 exponentials in fp32; P
+      // carries their bf16 rounding (a relative 2^-9 per term, unbiased).
       const float negm = m_ref == -INFINITY ? 0.f : -m_ref;   // all-masked rows: every s is -inf
       float ls8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t v[32];
-        tmem_ld32(tmem + st * kKT + hf * 32 + lane_off, v);
-        tmem_ld_wait();
-        if (!full_tile) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (k0 + hf * 32 + c > pos) v[c] = __float_as_uint(-INFINITY);
-        }
         uint32_t pw[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           // exponents in fp32, 2^x as an f16 pair, then bf16 for the product
-          const __half2 xh = __floats2half2_rn(fmaf(__uint_as_float(v[2 * c]), p.qscale, negm),
-                                               fmaf(__uint_as_float(v[2 * c + 1]), p.qscale, negm));
+          const __half2 xh = __floats2half2_rn(fmaf(__uint_as_float(v[hf][2 * c]), p.qscale, negm),
+                                               fmaf(__uint_as_float(v[hf][2 * c + 1]), p.qscale, negm));
           const uint32_t eh = ex2_f16x2(*reinterpret_cast<const uint32_t*>(&xh));
           const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&eh));
           const __nv_bfloat162 pk = __floats2bfloat162_rn(pf.x, pf.y);
-          ls8[(2 * c) & 7] += __low2float(pk);
-          ls8[(2 * c + 1) & 7] += __high2float(pk);
+          ls8[(2 * c) & 7] += pf.x;
+          ls8[(2 * c + 1) & 7] += pf.y;
           pw[c] = *reinterpret_cast<const uint32_t*>(&pk);
         }
         tmem_st16(tmem + st * kKT + hf * 16 + lane_off, pw);
