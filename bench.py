@@ -70,6 +70,24 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x, world, device):
+    """The largest value of x over all ranks (the slowest rank's time); x
+    itself for one rank.  Works with any process-group backend."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, total_ms, steps, world):
+    """Whole-job throughput: the units all ranks processed (each rank runs the
+    same workload on its own replica) over the slowest rank's time."""
+    return world * units_per_rank / (total_ms / 1e3 / steps)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -547,11 +565,7 @@ def run_prefill(args, rank, world, local_rank):
     stop.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    total_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     assert pa.last_error() == 0
     step_s = total_ms / 1e3 / K
     tflops = world * flops / step_s / 1e12
@@ -563,7 +577,7 @@ def run_prefill(args, rank, world, local_rank):
         stream, {"q": q.cpu().pin_memory()}, out,
         lambda d, o: pa.prefill(o, d["q"], case["k_cache"], case["v_cache"], case["block_tables"],
                                 case["context_lens"], case["scale"]), Ke)
-    e2e_s = e2e_ms / 1e3 / Ke
+    e2e_s = max_over_ranks(e2e_ms, world, dev) / 1e3 / Ke
     if rank != 0:
         return
     peak, src = tensor_peak()
@@ -639,8 +653,8 @@ def run_swap(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     assert pa.last_error() == 0
-    ms = e[0].elapsed_time(e[1]) / K
-    value = world * moved / (ms / 1e3) / 1e9
+    ms = max_over_ranks(e[0].elapsed_time(e[1]), world, dev) / K
+    value = whole_job_rate(moved, ms, 1, world) / 1e9
     # copy engine, same bytes, contiguous, both directions
     flat_d = k[:n].view(-1)
     flat_h = hk.view(-1)
@@ -752,7 +766,7 @@ def run_mixed(args, rank, world, local_rank):
                            else local_rank)
     sampler.start()
     time.sleep(0.25)
-    ms = timed(step, K)
+    ms = max_over_ranks(timed(step, K), world, dev)
     clocks = sampler.stop()
     assert pa.last_error() == 0
     split_ms = timed(split_step, K)
@@ -761,7 +775,7 @@ def run_mixed(args, rank, world, local_rank):
         stream, {"q": q.cpu().pin_memory()}, out,
         lambda d, o: pa.prefill_varlen(o, d["q"], case["query_start"], case["k_cache"], case["v_cache"],
                                        case["block_tables"], case["context_lens"], case["scale"]), min(K, 100))
-    e2e_ms /= min(K, 100)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev) / min(K, 100)
     if rank != 0:
         return
     peak, src = tensor_peak()
@@ -869,15 +883,11 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     if world > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(stop)
+    total_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     dec_ms = statistics.mean(d0[i].elapsed_time(d1[i]) for i in range(K))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     assert pa.last_error() == 0, "device-detected error in the timed region"
     step_s = total_ms / 1e3 / K
-    value = world * step_bytes / step_s / 1e9
+    value = whole_job_rate(step_bytes, total_ms, K, world) / 1e9
 
     # the same step captured once as a CUDA graph and replayed K times
     graph_line = None
@@ -930,11 +940,8 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     Ke = min(K, 1000)
     e2e_ms, e2e_last, h2d, d2h = pipelined_e2e(stream, host, out, e2e_compute, Ke)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_bytes / (e2e_ms / 1e3 / Ke) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = whole_job_rate(step_bytes, e2e_ms, Ke, world) / 1e9
     # the pipelined results equal the device-resident step's
     assert torch.equal(e2e_last, out.cpu()), "end-to-end result differs from the device-resident step"
 
