@@ -107,6 +107,13 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Transpose an 8x8 matrix of 16-bit values held in mma fragment layout
+// (lane g*4+q holds row g, columns 2q and 2q+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -415,7 +422,214 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     }
     const int h0 = (item.kvh0 + hl) * p.G + item.sg * GT;
 
-    if constexpr (MMA && SCALED) {
+    if constexpr (MMA && SCALED && GT <= 8) {
+      // e4m3 pool, query group of at most 8 heads: tokens in the M rows.
+      // S^T = K Q^T with the 16 tokens of a k-step as M and the query heads
+      // as N (8 columns), then O^T = V^T P with head dims as M and heads as N:
+      //  * K codes come through ldmatrix as byte pairs (a lane gets dims
+      //    4tq..4tq+3 of a 16-dim chunk of one token) and form the A
+      //    fragment; the k-step's reduction index is permuted the same way
+      //    in the Q^T fragment (slots 2tq,2tq+1 <-> dims 4tq,4tq+1; slots
+      //    2tq+8,2tq+9 <-> dims 4tq+2,4tq+3);
+      //  * V codes come through ldmatrix.trans; one byte permute splits a
+      //    lane's codes into even-dim and odd-dim pairs, so each 16-dim chunk
+      //    is one M tile whose rows g and g+8 are dims 2g and 2g+1;
+      //  * P^T (tokens x heads, the S^T accumulator) becomes the B operand
+      //    through an in-register 8x8 transpose (movmatrix);
+      //  * Q, the K and V scales and the f16 range of P are handled as on
+      //    the query-rows-in-M path (power-of-two Q scaling, per-token K
+      //    scale on the scores, V scale relative to a running power-of-two
+      //    reference on P).
+      constexpr int KS = D / 16;       // k-steps of S^T
+      constexpr int MT = D / 16;       // M tiles of O^T (16 dims each)
+      const int g = lane >> 2, tq = lane & 3;
+      const bool hv = g < GT;          // this lane's Q^T column (head g) is a real head
+      const uint2* qp = reinterpret_cast<const uint2*>(
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + (hv ? g : 0)) * QROW);
+      uint2 qraw[KS];
+      float qmax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qraw[kk] = hv ? __ldg(qp + kk * 4 + tq) : make_uint2(0u, 0u);    // dims 16kk+4tq .. +3
+        qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(bf16lo(qraw[kk].x)), fabsf(bf16hi(qraw[kk].x))),
+                                 fmaxf(fabsf(bf16lo(qraw[kk].y)), fabsf(bf16hi(qraw[kk].y)))));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+      int qe = 0;
+      if (qmax > 0.f) qe = max(-100, min(100, ilogbf(qmax) - 14));
+      const float qdown = ldexpf(1.f, -qe);
+      uint32_t qb[KS][2];
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qb[kk][0] = pack_f16(bf16lo(qraw[kk].x) * qdown, bf16hi(qraw[kk].x) * qdown);
+        qb[kk][1] = pack_f16(bf16lo(qraw[kk].y) * qdown, bf16hi(qraw[kk].y) * qdown);
+      }
+      const float sfac = p.qscale * ldexpf(1.f, qe);
+      float OT[MT][4];               // rows: dims 16c+2g (0,1) and 16c+2g+1 (2,3); columns: heads 2tq, 2tq+1
+#pragma unroll
+      for (int c = 0; c < MT; ++c) OT[c][0] = OT[c][1] = OT[c][2] = OT[c][3] = 0.f;
+      float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};   // heads 2tq, 2tq+1 (partial l per lane)
+      int rexp = -1000;
+
+      const int nblk = item.je - item.jb;
+      for (int i = gw; i < nblk; i += WPH, ++wcount) {
+        uint32_t ph;
+        const int st = gw * SPW + ring(wcount, ph);
+        bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        if (live) {
+          const bool late = !mbar_wait(&full[st], ph);
+          if (__any_sync(0xffffffffu, late)) {
+            live = false;
+            if (lane == 0) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          }
+        }
+        if (live) {
+          const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
+          unsigned char* vt_ptr = tilesV + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
+          const uint32_t kt = smem_u32(tilesK + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes);
+          const uint32_t vt = smem_u32(vt_ptr);
+          const float* sk = sclK + st * p.bs;
+          const float* sv = sclV + st * p.bs;
+          if (valid < p.bs) {
+            for (int idx = lane; idx < (p.bs - valid) * 8; idx += 32)
+              *reinterpret_cast<uint4*>(vt_ptr + (valid + idx / 8) * 128 + (idx % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          float vmax = 0.f;
+          for (int t = lane; t < valid; t += 32) vmax = fmaxf(vmax, sv[t]);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+          if (vmax > 0.f) {
+            const int ve = ilogbf(vmax) + 1;
+            if (ve > rexp) {
+              if (rexp > -1000) {
+                const float f = ldexpf(1.f, rexp - ve);
+#pragma unroll
+                for (int c = 0; c < MT; ++c) {
+                  OT[c][0] *= f;
+                  OT[c][1] *= f;
+                  OT[c][2] *= f;
+                  OT[c][3] *= f;
+                }
+              }
+              rexp = ve;
+            }
+          }
+          const float vdown = rexp > -1000 ? ldexpf(1.f, -rexp) : 0.f;
+          for (int tb = 0; tb < valid; tb += 16) {
+            // S^T: rows tokens tb+g, tb+g+8; columns heads 2tq, 2tq+1
+            float St[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+              // lanes 0-7: tokens tb..+7, chunk 2kp; 8-15: tokens tb+8..+15,
+              // chunk 2kp; 16-31: the same for chunk 2kp+1
+              const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
+#pragma unroll
+              for (int kp = 0; kp < KS / 2; ++kp) {
+                const int c = 2 * kp + (lane >> 4);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kt + tt * 128 + ((c ^ (tt & 7)) << 4), r0, r1, r2, r3);
+                uint32_t a[2][4];
+                e4m3x4_to_f16x2x2(r0, a[0][0], a[0][2]);    // tokens 0-7: dims 4tq..+1, 4tq+2..+3
+                e4m3x4_to_f16x2x2(r1, a[0][1], a[0][3]);    // tokens 8-15
+                e4m3x4_to_f16x2x2(r2, a[1][0], a[1][2]);
+                e4m3x4_to_f16x2x2(r3, a[1][1], a[1][3]);
+                mma_f16_16816(St, a[0], qb[2 * kp][0], qb[2 * kp][1]);
+                mma_f16_16816(St, a[1], qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+              }
+            }
+            const int t0 = tb + g, t1 = tb + g + 8;
+            const bool ok0 = t0 < valid, ok1 = t1 < valid;
+            const float f0 = ok0 ? sfac * sk[t0] : 0.f, f1 = ok1 ? sfac * sk[t1] : 0.f;
+            St[0] = ok0 ? St[0] * f0 : -INFINITY;
+            St[1] = ok0 ? St[1] * f0 : -INFINITY;
+            St[2] = ok1 ? St[2] * f1 : -INFINITY;
+            St[3] = ok1 ? St[3] * f1 : -INFINITY;
+            float alpha[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(St[e], St[2 + e]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float mn = fmaxf(mh[e], mx);
+              alpha[e] = mn == -INFINITY ? 1.f : exp2f(mh[e] - mn);
+              mh[e] = mn;
+              lh[e] *= alpha[e];
+            }
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+              for (int c = 0; c < MT; ++c) {
+                OT[c][0] *= alpha[0];
+                OT[c][1] *= alpha[1];
+                OT[c][2] *= alpha[0];
+                OT[c][3] *= alpha[1];
+              }
+            }
+            const float vs0 = ok0 ? sv[t0] * vdown : 0.f, vs1 = ok1 ? sv[t1] * vdown : 0.f;
+            float pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float pk = St[e] == -INFINITY ? 0.f : exp2f(St[e] - mh[e & 1]);
+              lh[e & 1] += pk;
+              pw[e] = pk * (e < 2 ? vs0 : vs1);
+            }
+            // P^T as the B operand: transpose the two 8x8 (tokens x heads) halves
+            const uint32_t b0 = movmatrix_t(pack_f16(pw[0], pw[1]));   // tokens 0-7
+            const uint32_t b1 = movmatrix_t(pack_f16(pw[2], pw[3]));   // tokens 8-15
+            {
+              // ldmatrix.trans: lanes 0-7 tokens tb..+7, 8-15 tokens tb+8..+15
+              // (chunk 2j); lanes 16-31 the same for chunk 2j+1
+              const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
+#pragma unroll
+              for (int j = 0; j < D / 32; ++j) {
+                const int c = 2 * j + (lane >> 4);
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(vt + tt * 128 + ((c ^ (tt & 7)) << 4), r0, r1, r2, r3);
+                uint32_t a0[4], a1[4];   // {even dims tokens 0-7, odd dims tokens 0-7, even 8-15, odd 8-15}
+                e4m3x4_to_f16x2x2(__byte_perm(r0, 0u, 0x3120), a0[0], a0[1]);
+                e4m3x4_to_f16x2x2(__byte_perm(r1, 0u, 0x3120), a0[2], a0[3]);
+                e4m3x4_to_f16x2x2(__byte_perm(r2, 0u, 0x3120), a1[0], a1[1]);
+                e4m3x4_to_f16x2x2(__byte_perm(r3, 0u, 0x3120), a1[2], a1[3]);
+                mma_f16_16816(OT[2 * j], a0, b0, b1);
+                mma_f16_16816(OT[2 * j + 1], a1, b0, b1);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      // the row sums are split over the 8 lanes sharing tq
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 4);
+        lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 8);
+        lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 16);
+      }
+      const float vup = rexp > -1000 ? ldexpf(1.f, rexp) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * tq + e;
+        if (h < GT) {
+          float* dst = mbuf + (warp * GT + h) * (D + 2);
+#pragma unroll
+          for (int c = 0; c < MT; ++c) {
+            dst[16 * c + 2 * g] = OT[c][e] * vup;
+            dst[16 * c + 2 * g + 1] = OT[c][2 + e] * vup;
+          }
+          if (g == 0) {
+            dst[D] = mh[e];
+            dst[D + 1] = lh[e];
+          }
+        }
+      }
+    } else if constexpr (MMA && SCALED) {
       // e4m3 pool on tensor cores (f16 m16n8k16, fp32 accumulation), the
       // query group in the M rows as on the bf16 path.  Differences:
       //  * K codes are read with ldmatrix as byte pairs: a lane gets 4
