@@ -38,7 +38,7 @@ WORKLOAD_TEXT = {
     "c3": "bf16 MHA decode: 40 heads, head_dim 128, block_size 16, batch 128, context log-normal "
           "(median 512, cap 4096), scattered pool; plus reshape_and_cache of 128 new tokens",
     "c4": "bf16 GQA decode: 32/8 heads, head_dim 128, block_size 16, batch 256, context U[1024,32768], "
-          "split-K 512; plus reshape_and_cache of 256 new tokens",
+          "split-K over 2048-token partitions (automatic); plus reshape_and_cache of 256 new tokens",
     "c4b32": "as c4 with block_size 32",
     "c2fp8": "as c2 over an e4m3 K/V pool with per-token fp32 scales (codes + scales read per token); "
              "append quantises the 64 new tokens",

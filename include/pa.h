@@ -32,6 +32,12 @@
  *    K/V pools, queries and outputs must be 16-byte aligned.
  *  - `stream` is a cudaStream_t (NULL: the legacy default stream).  Every
  *    call only enqueues work on it and returns without synchronising.
+ *  - CUDA graphs: every argument the kernels read is a device pointer or a
+ *    size, so a captured call replays with whatever the pointed-to buffers
+ *    hold at replay time.  The first call with a new combination of sizes
+ *    and pool (kernel variant, tensor map) does host-side set-up (function
+ *    attributes, occupancy query, tensor-map encoding, cached afterwards):
+ *    make one call outside the capture first.
  *  - Return value: 0 on success, or a negative PA_ERR_* code when the host
  *    side rejects the arguments — in that case nothing was launched.
  *  - Conditions only the device can see (a block id outside the pool, a slot
@@ -108,7 +114,7 @@ int pa_reshape_and_cache(const void* key, const void* value,
  *   block_tables   [num_seqs, max_blocks_per_seq] int32
  *   context_lens   [num_seqs] int32
  *   scale          the pages use 1/sqrt(head_dim)
- *   partition_size split-K partition in tokens: 0 = automatic (512 tokens
+ *   partition_size split-K partition in tokens: 0 = automatic (256 tokens
  *                  when num_heads == num_kv_heads, 2048 for grouped-query
  *                  attention), < 0 = never split, > 0 = a multiple of
  *                  block_size.  A sequence longer

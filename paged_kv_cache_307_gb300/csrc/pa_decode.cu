@@ -148,12 +148,13 @@ int fp8_heads_per_item(int num_kv_heads) {
   return hg;
 }
 
-// Automatic split: 512-token partitions for MHA (G = 1), 2048 for GQA, whose
+// Automatic split: 256-token partitions for MHA (G = 1; finer items balance
+// the persistent grid better than 512: c2 +0.5 %, c3 +1.3 %), 2048 for GQA, whose
 // items already cover several query heads per K/V read.
 int resolve_partition(int max_blocks, int bs, int partition_size, int G) {
   const int max_ctx = max_blocks * bs;
   if (partition_size < 0) return max_ctx;
-  int P = partition_size > 0 ? partition_size : (G >= 2 ? 2048 : 512);
+  int P = partition_size > 0 ? partition_size : (G >= 2 ? 2048 : 256);
   if (P >= max_ctx) P = max_ctx;
   return P;
 }

@@ -180,11 +180,13 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, 
 // e4m3 tensor-core instances are held to three CTAs per SM (at most 136
 // registers): their per-block conversion work needs the extra warps to hide
 // latency (20 % faster on the grouped-query workload than two CTAs per SM).
+// Groups of 16 (query rows in M, 64 accumulator registers) get two, which
+// they fill without spilling.
 #ifndef PA_FP8_MMA_MIN_BLOCKS
 #define PA_FP8_MMA_MIN_BLOCKS 3
 #endif
 template <typename T, typename KT, int D, int GT, bool MMA, int HG>
-__global__ void __launch_bounds__(kThreads, (MMA && sizeof(KT) == 1) ? PA_FP8_MMA_MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(kThreads, (MMA && sizeof(KT) == 1) ? (GT <= 8 ? PA_FP8_MMA_MIN_BLOCKS : 2) : 1)
 decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
               const DecodeParams p) {
   using E = Elem<T>;                           // queries and output

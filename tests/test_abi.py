@@ -29,9 +29,9 @@ def test_version_and_error_text(pa):
 
 
 def test_workspace_and_partition_arithmetic(pa):
-    # 64 seqs x 32 heads, 128 blocks of 16 -> 2048 tokens -> 4 partitions of 512
-    assert pa.partition_size(64, 32, 32, 128, 128, 16, 0) == 512
-    rows = 64 * 32 * 4
+    # 64 seqs x 32 heads, 128 blocks of 16 -> 2048 tokens -> 8 partitions of 256
+    assert pa.partition_size(64, 32, 32, 128, 128, 16, 0) == 256
+    rows = 64 * 32 * 8
     ml = (rows * 8 + 255) // 256 * 256
     assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, 0) == ml + rows * 128 * 4
     assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, -1) == 0          # never split
