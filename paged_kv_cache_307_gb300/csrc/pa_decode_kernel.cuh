@@ -863,6 +863,150 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
           }
         }
       }
+    } else if constexpr (MMA && GT <= 8) {
+      // bf16 pool, query group of at most 8 heads: tokens in the M rows.
+      // S^T = K Q^T (M = 16 tokens, N = 8 heads) with K rows straight from
+      // ldmatrix as the A fragment; O^T = V^T P (M = 16 head dims, N = heads)
+      // with V^T from ldmatrix.trans and P^T turned into the B operand by an
+      // in-register 8x8 transpose.  Half the MMAs of the query-rows-in-M
+      // formulation for groups of up to 8, and O^T in 32 registers.
+      constexpr int KS = D / 16;       // k-steps of S^T
+      constexpr int MT = D / 16;       // M tiles of O^T
+      const int g = lane >> 2, tq = lane & 3;
+      const bool hv = g < GT;
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+          static_cast<const unsigned char*>(p.q) + ((size_t)item.b * p.Hq + h0 + (hv ? g : 0)) * QROW);
+      uint32_t qb[KS][2];             // Q^T B fragment: head g, dims 16kk+2tq..+1 and 16kk+2tq+8..+9
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qb[kk][0] = hv ? __ldg(qp + kk * 8 + tq) : 0u;
+        qb[kk][1] = hv ? __ldg(qp + kk * 8 + 4 + tq) : 0u;
+      }
+      float OT[MT][4];               // rows: dims 16m+g (0,1) and 16m+8+g (2,3); columns: heads 2tq, 2tq+1
+#pragma unroll
+      for (int m = 0; m < MT; ++m) OT[m][0] = OT[m][1] = OT[m][2] = OT[m][3] = 0.f;
+      float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};
+      const uint32_t half_bytes = (uint32_t)p.bs * 128u;
+
+      const int nblk = item.je - item.jb;
+      for (int i = gw; i < nblk; i += WPH, ++wcount) {
+        uint32_t ph;
+        const int st = gw * SPW + ring(wcount, ph);
+        bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        if (live) {
+          const bool late = !mbar_wait(&full[st], ph);
+          if (__any_sync(0xffffffffu, late)) {
+            live = false;
+            if (lane == 0) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          }
+        }
+        if (live) {
+          const int valid = min(p.bs, item.t1 - (item.jb + i) * p.bs);
+          unsigned char* vt_ptr = tilesV + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes;
+          const uint32_t kt = smem_u32(tilesK + (size_t)st * stage_bytes + (size_t)hl * p.tile_bytes);
+          const uint32_t vt = smem_u32(vt_ptr);
+          if (valid < p.bs) {
+            // slots past the context may hold anything: clear those V rows
+            for (int idx = lane; idx < (p.bs - valid) * (D / 8); idx += 32) {
+              const int t = valid + idx / (D / 8), c = idx % (D / 8);
+              *reinterpret_cast<uint4*>(vt_ptr + (c >> 3) * half_bytes + t * 128 + (c & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          for (int tb = 0; tb < valid; tb += 16) {
+            float St[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+              // lanes 0-7: tokens tb..+7, chunk 2kk; 8-15: tokens tb+8..+15,
+              // chunk 2kk; 16-31: the same for chunk 2kk+1 (8 dims per chunk)
+              const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
+#pragma unroll
+              for (int kk = 0; kk < KS; ++kk) {
+                const int c = 2 * kk + (lane >> 4);
+                uint32_t a[4];
+                ldsm_x4(kt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), a[0], a[1], a[2], a[3]);
+                mma_bf16_16816(St, a, qb[kk][0], qb[kk][1]);
+              }
+            }
+            const int t0 = tb + g, t1 = tb + g + 8;
+            const bool ok0 = t0 < valid, ok1 = t1 < valid;
+            St[0] = ok0 ? St[0] * p.qscale : -INFINITY;
+            St[1] = ok0 ? St[1] * p.qscale : -INFINITY;
+            St[2] = ok1 ? St[2] * p.qscale : -INFINITY;
+            St[3] = ok1 ? St[3] * p.qscale : -INFINITY;
+            float alpha[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(St[e], St[2 + e]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float mn = fmaxf(mh[e], mx);
+              alpha[e] = mn == -INFINITY ? 1.f : exp2f(mh[e] - mn);
+              mh[e] = mn;
+              lh[e] *= alpha[e];
+            }
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                OT[m][0] *= alpha[0];
+                OT[m][1] *= alpha[1];
+                OT[m][2] *= alpha[0];
+                OT[m][3] *= alpha[1];
+              }
+            }
+            float pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pw[e] = St[e] == -INFINITY ? 0.f : exp2f(St[e] - mh[e & 1]);
+              lh[e & 1] += pw[e];
+            }
+            const uint32_t b0 = movmatrix_t(pack_bf16(pw[0], pw[1]));   // tokens 0-7
+            const uint32_t b1 = movmatrix_t(pack_bf16(pw[2], pw[3]));   // tokens 8-15
+            {
+              // ldmatrix.trans: lanes 0-7 tokens tb..+7 chunk 2m; 8-15 the
+              // same tokens, chunk 2m+1; 16-31 tokens tb+8..+15, chunks 2m, 2m+1
+              const int tt = min(tb + (lane & 7) + ((lane >> 4) << 3), p.bs - 1);
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                const int c = 2 * m + ((lane >> 3) & 1);
+                uint32_t a[4];
+                ldsm_x4_t(vt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), a[0], a[1], a[2],
+                          a[3]);
+                mma_bf16_16816(OT[m], a, b0, b1);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 4);
+        lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 8);
+        lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 16);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * tq + e;
+        if (h < GT) {
+          float* dst = mbuf + (warp * GT + h) * (D + 2);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            dst[16 * m + g] = OT[m][e];
+            dst[16 * m + 8 + g] = OT[m][2 + e];
+          }
+          if (g == 0) {
+            dst[D] = mh[e];
+            dst[D + 1] = lh[e];
+          }
+        }
+      }
     } else if constexpr (MMA) {
       // Query heads h0..h0+GT-1 are the M rows of m16n8k16 (rows >= GT are
       // zero); K rows are the N columns of S = Q K^T, and P (bf16) times V
