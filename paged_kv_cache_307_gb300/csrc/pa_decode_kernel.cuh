@@ -11,29 +11,42 @@
 // of exponentials and a rescaled output, normalised at the end.
 //
 // How (GB300):
-//  * Work item = (sequence, KV head, query-head subgroup, partition of P
-//    tokens).  A persistent grid (resident CTAs x SMs) strides over the item
-//    space; the sequence index is innermost so CTAs running side by side read
-//    the same blocks when sequences share a prompt.
+//  * Work item = (sequence, partition of P tokens, group of HG KV heads,
+//    query-head subgroup).  A persistent grid (resident CTAs x SMs) strides
+//    over the items.  With up to kDenseMaxSeqs sequences every CTA first
+//    builds the clamped lengths and the prefix sum of partitions per sequence
+//    in shared memory and numbers only the real items, sequence by sequence
+//    (the HG-group / subgroup index innermost), so each CTA gets the same
+//    number of items up to one; beyond that a sparse index over max_parts
+//    partitions is used.
 //  * Each CTA = 1 producer warp + kConsumerWarps consumer warps.  The producer
-//    reads the item's block-table entries with one coalesced warp load, then
-//    issues, per block, two TMA tensor loads (box {D, 1 head, bs, 1 block} of
-//    the [NB, bs, Hkv, D] pool) for K and V into a ring of shared-memory
-//    stages, completing on an mbarrier with transaction bytes.  A block id
-//    outside the pool is flagged and replaced by block 0, so no copy leaves
-//    the pool.
-//  * Consumer warps take the item's blocks round-robin, and each warp owns its
-//    own ring of SPW stages which it consumes strictly in order (a ring shared
-//    by several round-robin consumers lets a warp wait on a stage two phases
-//    ahead, where a parity wait matches the stale phase).  Inside a warp, LPT
-//    lanes share one token (each lane owns two 16-byte chunks of head_dim), so
-//    one warp covers TPW tokens per pass with conflict-free 16-byte shared
-//    loads.  Each lane group keeps its own online-softmax state (m, l, o) for
-//    its tokens; group, warp and partition states are merged by log-sum-exp at
-//    the end, which is exact up to rounding (the update is associative).
-//  * Scores are computed in the base-2 domain (q pre-multiplied by
-//    scale*log2 e), with exp2f.  The K/V rows are read once from HBM and used
-//    for all GT query heads of the subgroup (GQA) straight from registers.
+//    reads an item's block-table entries with one coalesced warp load, then
+//    per block arms a stage's mbarrier (lane 0) and issues the block's TMA
+//    tensor loads from parallel lanes: one box {D, HG heads, bs, 1 block} each
+//    for K and V on the CUDA-core path, 128-byte-swizzled 128-byte column
+//    spans on the tensor-core paths, plus the two scale rows of an e4m3 pool
+//    (untiled bulk copies).  A block id outside the pool is flagged and
+//    replaced by block 0, so no copy leaves the pool.
+//  * Consumer warp w works on head w % HG of the item in warp group w / HG;
+//    block i of an item goes to group i % (kConsumerWarps / HG), and every
+//    group owns its own ring of SPW stages, consumed strictly in order by all
+//    its warps (a ring shared by round-robin consumers lets a warp wait on a
+//    stage two phases ahead, where a parity wait matches the stale phase).
+//  * Consumers, by pool and group size:
+//      - CUDA cores (MHA, fp32, e4m3 MHA, odd groups): LPT lanes share one
+//        token, each owning one or two 16-byte chunks of head_dim; scores in
+//        the base-2 domain (q pre-multiplied by scale*log2 e), exp2f, one
+//        online-softmax state per lane group;
+//      - tensor cores, tokens in M (bf16 and e4m3, groups of up to 8):
+//        S^T = K Q^T with the 16 tokens of a k-step as the M rows and the
+//        heads as N = 8, P^T transposed in registers (movmatrix) into the B
+//        operand of O^T = V^T P;
+//      - tensor cores, query rows in M (groups of 16): S = Q K^T with the
+//        query group as the M rows of m16n8k16.
+//    e4m3 codes are converted exactly (cvt.rn.f16x2.e4m3x2); the per-token K
+//    scale multiplies the score and the V scale the softmax weight.  Lane
+//    groups, warp groups and partitions are merged by log-sum-exp, exact up to
+//    rounding (the update is associative).
 //  * A sequence whose context fits one partition is normalised and written
 //    directly; longer ones write (m, l, unnormalised o) per partition to the
 //    workspace, and merge_kernel combines them.
