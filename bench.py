@@ -827,7 +827,7 @@ def run_ours(args, rank, world, local_rank):
     ws = pa.alloc_workspace(case.q, case.k_cache, case.block_tables, args.partition)
     out = torch.empty_like(case.q)
     stream = torch.cuda.current_stream()
-    P = pa.partition_size(Bsz, Hq, spec.Hkv, D, case.max_blocks, spec.bs, args.partition)
+    P = pa.partition_size(Bsz, Hq, spec.Hkv, D, case.max_blocks, spec.bs, args.partition, fp8=fp8)
     launches_per_step = 2 + (1 if case.max_blocks * spec.bs > P else 0)
 
     dec_bytes = W.algorithmic_decode_bytes(case)

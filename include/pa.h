@@ -183,7 +183,14 @@ int pa_reshape_and_cache_fp8(const void* key, const void* value,
  *   query, out        dtype must be PA_BF16
  *   k_cache, v_cache  e4m3 pools; k_scale, v_scale as written by
  *                     pa_reshape_and_cache_fp8 (16-byte aligned)
- *   other arguments   as for pa_decode; the workspace size is the same
+ *   partition_size    as for pa_decode, but the automatic choice is 512
+ *                     tokens when num_heads == num_kv_heads (2048 for
+ *                     grouped-query attention); pa_decode_fp8_partition_size
+ *                     returns the size used
+ *   workspace         pa_decode_workspace_bytes() with the same sizes is
+ *                     enough (the automatic partition here is never shorter
+ *                     than pa_decode's, so no more partials are written)
+ *   other arguments   as for pa_decode
  *
  * Query groups of 2 to 16 heads with head_dim 128 and block_size >= 8 run
  * on tensor cores: f16 m16n8k16 products of the exactly converted codes with
@@ -267,6 +274,10 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, 
 /* The partition size (tokens) pa_decode will use for these arguments. */
 int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                              int max_blocks_per_seq, int block_size, int partition_size);
+
+/* The partition size (tokens) pa_decode_fp8 will use for these arguments. */
+int pa_decode_fp8_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_size);
 
 /*
  * Copy-on-write block copy.  [KVS] Fig 19-8 and [OS] §四: before a sequence

@@ -37,6 +37,8 @@ lib.pa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 lib.pa_decode_workspace_bytes.restype = _sz
 lib.pa_decode_partition_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 lib.pa_decode_partition_size.restype = _i
+lib.pa_decode_fp8_partition_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+lib.pa_decode_fp8_partition_size.restype = _i
 lib.pa_copy_blocks.argtypes = [_p, _p, _i64p, _i, _i, _i, _i, _i, _i, _p]
 lib.pa_copy_blocks.restype = _i
 lib.pa_prefill_paged.argtypes = [_p, _p, _i, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _p]
@@ -133,9 +135,10 @@ def workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, blo
                                          block_size, partition_size)
 
 
-def partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, partition_size=0):
-    return lib.pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
-                                        block_size, partition_size)
+def partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, partition_size=0,
+                   fp8=False):
+    f = lib.pa_decode_fp8_partition_size if fp8 else lib.pa_decode_partition_size
+    return f(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, partition_size)
 
 
 def alloc_workspace(q, k_cache, block_tables, partition_size=0):

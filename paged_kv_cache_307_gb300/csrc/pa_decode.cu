@@ -148,13 +148,15 @@ int fp8_heads_per_item(int num_kv_heads) {
   return hg;
 }
 
-// Automatic split: 256-token partitions for MHA (G = 1; finer items balance
-// the persistent grid better than 512: c2 +0.5 %, c3 +1.3 %), 2048 for GQA, whose
-// items already cover several query heads per K/V read.
-int resolve_partition(int max_blocks, int bs, int partition_size, int G) {
+// Automatic split: 2048 tokens for GQA, whose items already cover several
+// query heads per K/V read; for MHA 256 tokens over 16-bit pools (finer items
+// balance the persistent grid better than 512: c2 +0.5 %, c3 +1.3 %) and 512
+// over e4m3 pools, where an item's fixed costs (table read, lane and warp
+// merges, the partial's write) weigh on half the bytes (c2 over e4m3: +7 %).
+int resolve_partition(int max_blocks, int bs, int partition_size, int G, bool fp8) {
   const int max_ctx = max_blocks * bs;
   if (partition_size < 0) return max_ctx;
-  int P = partition_size > 0 ? partition_size : (G >= 2 ? 2048 : 256);
+  int P = partition_size > 0 ? partition_size : (G >= 2 ? 2048 : fp8 ? 512 : 256);
   if (P >= max_ctx) P = max_ctx;
   return P;
 }
@@ -172,13 +174,25 @@ unsigned fetch_status_decode() {
 
 using namespace pa;
 
-extern "C" int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                                        int max_blocks_per_seq, int block_size, int partition_size) {
+static int partition_size_impl(bool fp8, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int max_blocks_per_seq, int block_size, int partition_size) {
   (void)num_seqs; (void)head_dim;
   if (max_blocks_per_seq <= 0 || !supported_block_size(block_size)) return PA_ERR_SHAPE;
   if (partition_size > 0 && partition_size % block_size) return PA_ERR_SHAPE;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return PA_ERR_SHAPE;
-  return resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads);
+  return resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads, fp8);
+}
+
+extern "C" int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int block_size, int partition_size) {
+  return partition_size_impl(false, num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                             partition_size);
+}
+
+extern "C" int pa_decode_fp8_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                            int max_blocks_per_seq, int block_size, int partition_size) {
+  return partition_size_impl(true, num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                             partition_size);
 }
 
 extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
@@ -216,7 +230,8 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
   if (fp8 && (!aligned16(k_scale) || !aligned16(v_scale))) return PA_ERR_ALIGN;
 
-  const int P = resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads);
+  const int P = resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads,
+                                  kv == PA_FP8_E4M3);
   const long long max_ctx = (long long)max_blocks_per_seq * block_size;
   const int max_parts = (int)((max_ctx + P - 1) / P);
   const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,

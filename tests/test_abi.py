@@ -37,6 +37,12 @@ def test_workspace_and_partition_arithmetic(pa):
     assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, -1) == 0          # never split
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 0) == 12                   # fits one partition
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 6) == -2                   # not a block multiple
+    # e4m3 pools: 512-token partitions for MHA, the same 2048 for grouped queries
+    assert pa.partition_size(64, 32, 32, 128, 128, 16, 0, fp8=True) == 512
+    assert pa.partition_size(64, 32, 8, 128, 128, 16, 0, fp8=True) == 2048
+    assert pa.partition_size(64, 32, 8, 128, 128, 16, 0) == 2048
+    assert pa.partition_size(64, 32, 32, 128, 128, 16, 64, fp8=True) == 64
+    assert pa.partition_size(1, 8, 8, 32, 3, 4, 0, fp8=True) == 12
 
 
 def test_host_side_rejections_launch_nothing(pa):
