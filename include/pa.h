@@ -131,8 +131,8 @@ int pa_reshape_and_cache(const void* key, const void* value,
  * the G query heads of a KV head are computed together on tensor cores
  * (m16n8k16 bf16 products, fp32 accumulation; P is rounded to bf16 for the
  * P*V product): for G <= 8 the block's tokens are the M rows and the heads
- * the N columns, for G = 16 the heads are the M rows.  Everything else runs
- * on CUDA cores in fp32.
+ * the N columns; for G >= 16, subgroups of 16 heads are the M rows.
+ * Everything else runs on CUDA cores in fp32.
  */
 int pa_decode(void* out, const void* query,
               const void* k_cache, const void* v_cache,
@@ -192,8 +192,8 @@ int pa_reshape_and_cache_fp8(const void* key, const void* value,
  *                     than pa_decode's, so no more partials are written)
  *   other arguments   as for pa_decode
  *
- * Query groups of 2 to 16 heads with head_dim 128 and block_size >= 8 run
- * on tensor cores: f16 m16n8k16 products of the exactly converted codes with
+ * Power-of-two query groups (G >= 2; subgroups of 16 above 16) with
+ * head_dim 128 and block_size >= 8 run on tensor cores: f16 m16n8k16 products of the exactly converted codes with
  * fp32 accumulation, Q scaled per work item by a power of two into f16
  * range, P carrying the V scale relative to a power-of-two reference (f16,
  * in [0, 1]).  Everything else runs on CUDA cores in fp32.
