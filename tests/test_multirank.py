@@ -80,3 +80,11 @@ def test_reference_arm_under_two_ranks_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    # the line carries the same metric and workload as the CUDA arm, and the
+    # oracle's own timing as both its cpu_baseline and its end-to-end figure
+    assert d["metric"].startswith("paged decode attention HBM GB/s") and d["unit"] == "GB/s"
+    assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 0
+    assert d["config"]["workload"].startswith("c2")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
