@@ -369,6 +369,20 @@ const char* pa_last_host_error(void);
 /* Human-readable text for a PA_ERR_* code or a PA_DEV_* bit. */
 const char* pa_strerror(int code);
 
+/*
+ * Health check of the bounded pipeline waits (a library facility; the pages
+ * have no counterpart).  Every mbarrier wait in the decode and prefill
+ * kernels gives up after 2 s, sets PA_DEV_TIMEOUT and lets the kernel finish,
+ * so a stalled pipeline leaves the CUDA context usable and shows up in
+ * pa_last_error().  This call exercises that path on its own: it launches one
+ * 32-thread CTA that waits on a shared-memory mbarrier nothing arrives at,
+ * giving up after limit_ns nanoseconds (1 .. 2e9).  Once the launch has run,
+ * pa_last_error() includes PA_DEV_TIMEOUT.  Asynchronous on `stream`; touches
+ * no global memory other than the status bit.  A limit outside the range
+ * returns PA_ERR_SHAPE and launches nothing.
+ */
+int pa_selftest_bounded_wait(unsigned long long limit_ns, void* stream);
+
 /* Library ABI version (major*100 + minor). */
 int pa_version(void);
 

@@ -60,6 +60,8 @@ lib.pa_last_host_error.argtypes = []
 lib.pa_last_host_error.restype = ctypes.c_char_p
 lib.pa_version.argtypes = []
 lib.pa_version.restype = _i
+lib.pa_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, _p]
+lib.pa_selftest_bounded_wait.restype = _i
 
 
 class PAError(RuntimeError):
@@ -233,6 +235,12 @@ def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, stream=None):
     _check(lib.pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), dst_k.shape[0], _ptr(src_k), _ptr(src_v), src_k.shape[0],
                               _ptr(pairs), pairs.shape[0], bs, H, D, _dtype(dst_k), _stream(stream)),
            "pa_swap_blocks")
+
+
+def selftest_bounded_wait(limit_ns, stream=None):
+    """Launch the bounded-wait health check (one warp waits on an mbarrier
+    nothing arrives at, giving up after ``limit_ns``)."""
+    _check(lib.pa_selftest_bounded_wait(int(limit_ns), _stream(stream)), "pa_selftest_bounded_wait")
 
 
 def last_error():

@@ -93,8 +93,9 @@ extern "C" int pa_last_error(void) {
   const unsigned a = pa::fetch_status_cache_ops();
   const unsigned b = pa::fetch_status_decode() | pa::fetch_status_decode_fp8();
   const unsigned c = pa::fetch_status_prefill();
-  if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) return PA_ERR_CUDA;
-  return (int)(a | b | c);
+  const unsigned d = pa::fetch_status_selftest();
+  if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu || d == 0xffffffffu) return PA_ERR_CUDA;
+  return (int)(a | b | c | d);
 }
 
 extern "C" const char* pa_strerror(int code) {

@@ -68,6 +68,9 @@ def test_host_side_rejections_launch_nothing(pa):
     # prefill: head_dim 64 and non-positive scale are rejected
     assert L.pa_prefill_paged(fake, fake, 16, fake, fake, fake, 8, fake, 2, 8, 8, 64, 16, 10, 1.0, 1, null) == -2
     assert L.pa_prefill_paged(fake, fake, 16, fake, fake, fake, 8, fake, 2, 8, 8, 128, 16, 10, -1.0, 1, null) == -2
+    # bounded-wait health check: a limit of 0 or above 2 s is rejected
+    assert L.pa_selftest_bounded_wait(0, null) == -2
+    assert L.pa_selftest_bounded_wait(3_000_000_000, null) == -2
     # swap: null source pool, misaligned destination, unsupported block size
     assert L.pa_swap_blocks(fake, fake, 4, null, fake, 10, fake, 2, 16, 2, 64, 1, null) == -1
     assert L.pa_swap_blocks(odd, fake, 4, fake, fake, 10, fake, 2, 16, 2, 64, 1, null) == -4

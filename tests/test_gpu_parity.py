@@ -237,6 +237,25 @@ def test_bad_block_id_and_length_are_flagged(pa):
     assert pa.last_error() & pa.DEV_BAD_LEN
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable(pa):
+    # a pipeline wait that nothing will satisfy ends after its limit with
+    # PA_DEV_TIMEOUT, which the host reads; the next calls run normally
+    assert pa.last_error() == 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    pa.selftest_bounded_wait(20_000_000)           # 20 ms
+    t1.record()
+    torch.cuda.synchronize()
+    assert t0.elapsed_time(t1) >= 19.0              # it waited out its limit
+    assert pa.last_error() == pa.DEV_TIMEOUT
+    assert pa.last_error() == 0                     # the bit is cleared once read
+    c = _cuda_case("c2", small=True)
+    out = gpu_decode(c)
+    assert pa.last_error() == 0
+    assert_close(f64(out), oracle_decode(c), "bf16")
+
+
 def test_permuted_pool_gives_bit_identical_output(pa):
     c = _cuda_case("c4", small=True)
     out1 = gpu_decode(c)
