@@ -11,11 +11,13 @@
 //  * Rows = 128 (query position, head) pairs that share one KV head: QP =
 //    128/G positions x G query heads (GQA packing), so every K/V tile is
 //    loaded once for all G heads.  D = 128.
-//  * Warp 0 (TMA): the Q tile (two 64-column halves, 128-byte swizzle) once,
-//    then per 64-key tile the K and V rows of its physical blocks (box {64,
-//    1 head, bs, 1 block} per half) into a 2-stage ring; lane 0 arms the
+//  * Warp 0 (TMA, K): the Q tile (two 64-column halves, 128-byte swizzle)
+//    once, then per 64-key tile the K rows of its physical blocks (box {64,
+//    1 head, bs, 1 block} per half) into a 2-stage ring; warp 6 (TMA, V)
+//    loads the V rows the same way into a ring of its own.  Lane 0 arms a
 //    stage's mbarrier and the tile's loads are issued by parallel lanes (one
 //    warp instruction), since one thread issuing them in series was slow.
+//    A K stage is free once S of its tile is done, a V stage only after P V.
 //  * Warp 1 (MMA): allocates 256 TMEM columns (S buffers at columns 0 and 64,
 //    O at 128..255) and issues S_{j+1} = Q K_{j+1}^T (M = 128, N = 64,
 //    K = 128: 8 tcgen05.mma) before waiting for P_j, so the next tile's
@@ -26,11 +28,12 @@
 //    commits execute in issue order, which is what makes reusing an S
 //    buffer (and the P written over it) safe two tiles later.
 //  * Warps 2-5 (softmax): one thread per row loads its 64 scores from TMEM
-//    (tcgen05.ld 32x32b), applies the causal mask and scale (base 2), keeps
-//    a running max and sum, and writes P = exp2(s - m) back as packed bf16
-//    over the first 32 columns of the same S buffer (tcgen05.st); at the end
-//    it reads O back, divides by the sum and stores bf16 rows.
-//  * 98 KB of shared memory and 192 threads per CTA: two CTAs per SM, so one
+//    once (tcgen05.ld 32x32b) and keeps them in registers, applies the causal
+//    mask (diagonal tile only) and scale (base 2), keeps a running max and
+//    sum, and writes P = exp2(s - m), computed as f16 pairs, back as packed
+//    bf16 over the first 32 columns of the same S buffer (tcgen05.st); at the
+//    end it reads O back, divides by the sum and stores bf16 rows.
+//  * 98 KB of shared memory and 224 threads per CTA: two CTAs per SM, so one
 //    CTA's softmax overlaps the other's MMAs.
 //  * The running max used as the exponent reference only moves when a new
 //    maximum exceeds it by more than 2^8; then the row's O is rescaled in
