@@ -7,7 +7,9 @@
  *         §19.2.2 block pool / block table, Fig 19-5 block-wise attention,
  *         Fig 19-8 copy-on-write; §19.2.3 the simplified implementation
  *         (pool layout, slot writes, block-table append, paged attention with
- *         an online softmax checked against dense softmax attention).
+ *         an online softmax checked against dense softmax attention);
+ *         §19.2.4 KV quantisation (FP8); §19.2.6 swapping blocks to CPU
+ *         memory on preemption.
  *   [OS]  "LLM 推理引擎的内存管理与调度：PagedAttention、Prefix Cache 与
  *         Continuous Batching" (zhouzhq2021.github.io): §三 the kernel looks a
  *         logical block up in the block table and forms the physical address
@@ -22,8 +24,9 @@
  *  - Element type: PA_F32 or PA_BF16; K, V, Q and the output share it,
  *    except for the e4m3 pool calls (pa_reshape_and_cache_fp8,
  *    pa_decode_fp8), whose pools hold PA_FP8_E4M3 codes with fp32 scales.
- *    Arithmetic is fp32 whatever the storage type; bf16 results are rounded
- *    to nearest even.
+ *    Accumulation is fp32 whatever the storage type (the tensor-core forms
+ *    round their product operands as each call's description states); bf16
+ *    results are rounded to nearest even.
  *  - Supported sizes: head_dim in {32, 64, 128}; block_size in {4, 8, 16,
  *    32}; num_heads a multiple of num_kv_heads.  Query head h reads KV head
  *    h / (num_heads / num_kv_heads) (grouped-query attention).
