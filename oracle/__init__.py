@@ -11,7 +11,8 @@ Pages this oracle restates (cited by title and section everywhere below):
 * [KVS]  "19.2 KV Cache 系统化管理" (paper.xwysyy.cn, llm-fullstack-book 19_2):
   §19.2.2 block tables, Fig 19-6 lifecycle, Fig 19-8 copy-on-write;
   §19.2.3 the simplified implementation (block pool, block table, paged
-  attention with an online softmax, and its check against dense attention).
+  attention with an online softmax, and its check against dense attention);
+  §19.2.5 prefix sharing (``paged_decode_shared_prefix``).
 * [OS]   "LLM 推理引擎的内存管理与调度：PagedAttention、Prefix Cache 与
   Continuous Batching" (zhouzhq2021.github.io): §三 block-table diagram,
   §四 reference counts and copy-on-write, §8.1 chunked prefill.
@@ -41,6 +42,8 @@ from .attention import (  # noqa: F401
     paged_decode_split,
     paged_prefill,
     paged_prefill_varlen,
+    shared_prefix_groups,
+    paged_decode_shared_prefix,
 )
 from .cache_ops import reshape_and_cache, copy_blocks, swap_blocks  # noqa: F401
 from .quant import (  # noqa: F401

@@ -269,3 +269,107 @@ def paged_prefill_varlen(q, query_start, k_cache, v_cache, block_tables, context
                                    context_lens[b:b + 1], scale)[0]
     return out
 
+
+
+# ---------------------------------------------------------------- shared prefixes
+
+def shared_prefix_groups(block_tables, context_lens, block_size):
+    """Find the sequences that share a prompt's physical blocks.
+
+    [KVS] §19.2.2 (copy-on-write and prefix sharing) and §19.2.5: samples
+    drawn from one prompt point their block tables at the same physical
+    blocks for the prompt (reference count = number of samples); [OS] §四
+    names beam search and parallel sampling as the cases.  A group is a
+    maximal run of adjacent sequences whose first block is one and the same
+    full physical block; its shared length is the number of leading table
+    entries that all members hold in common, counting only blocks that every
+    member fills completely (at most floor(L_b / bs) for each member b).  A
+    sequence alone is a group of one with no shared blocks.
+
+    Returns (group_start [n+1], shared_blocks [n]) as int64 arrays."""
+    lens = [int(x) for x in context_lens]
+    B = len(lens)
+    starts = [0]
+    for b in range(1, B):
+        same = (lens[b] >= block_size and lens[b - 1] >= block_size
+                and int(block_tables[b][0]) == int(block_tables[b - 1][0]))
+        if not same:
+            starts.append(b)
+    starts.append(B)
+    shared = []
+    for g in range(len(starts) - 1):
+        members = range(starts[g], starts[g + 1])
+        if len(members) < 2:
+            shared.append(0)
+            continue
+        cap = min(lens[b] // block_size for b in members)
+        lead = starts[g]
+        n = 0
+        while n < cap and all(int(block_tables[b][n]) == int(block_tables[lead][n]) for b in members):
+            n += 1
+        shared.append(n)
+    return np.array(starts, dtype=np.int64), np.array(shared, dtype=np.int64)
+
+
+def _valid_groups(group_start, B):
+    gs = [int(x) for x in group_start]
+    return len(gs) >= 1 and gs[0] == 0 and gs[-1] == B and all(a <= b for a, b in zip(gs, gs[1:]))
+
+
+def paged_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
+                               group_start, shared_blocks):
+    """Decode of a batch whose sequences share prompt blocks, with each shared
+    block's keys and values read once for all the sequences of its group.
+
+    Sequences group_start[g] .. group_start[g+1]-1 form group g; they declare
+    that the first shared_blocks[g] entries of their block-table rows name the
+    same physical blocks ([KVS] §19.2.5, Fig 19-8: every sample's table points
+    at the prompt's blocks).  The shared part actually used is
+
+        S_g = min(shared_blocks[g], min over members b of floor(L_b / bs))
+
+    whole blocks (each member holds every one of them completely), taken from
+    the FIRST member's table row.  For each member b and query head h:
+
+      * the state (m, l, o) of the online softmax of [KVS] §19.2.3 over the
+        S_g * bs shared tokens (one partition, as in ``decode_partials``);
+      * the state over b's own tokens S_g * bs .. L_b - 1, read through b's
+        own table row;
+      * the two merged by ``merge_partials`` (the log-sum-exp combination);
+        a part with no tokens is left out, and a sequence with none at all
+        gives zeros.
+
+    When the members' rows really share those blocks this is exactly
+    ``paged_decode`` (the merge is the associativity of the online softmax).
+    A descriptor that does not cover the batch as non-decreasing runs from 0
+    to B is ignored (plain decode)."""
+    q = _as_f64(q)
+    B, Hq, D = q.shape
+    bs = k_cache.shape[1]
+    if not _valid_groups(group_start, B):
+        return paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    for g in range(len(group_start) - 1):
+        s0, s1 = int(group_start[g]), int(group_start[g + 1])
+        if s1 <= s0:
+            continue
+        S = min([int(shared_blocks[g])] + [int(context_lens[b]) // bs for b in range(s0, s1)])
+        S = max(S, 0)
+        Ts = S * bs
+        Ks, Vs = gather_context(k_cache, v_cache, block_tables[s0], Ts)
+        for b in range(s0, s1):
+            L = int(context_lens[b])
+            parts = []
+            if Ts > 0:
+                parts.append(decode_partials(q[b], Ks, Vs, scale, Ts))
+            if L > Ts:
+                Kf, Vf = gather_context(k_cache, v_cache, block_tables[b], L)
+                Kt, Vt = Kf[Ts:], Vf[Ts:]
+                parts.append(decode_partials(q[b], Kt, Vt, scale, L - Ts))
+            if not parts:
+                continue
+            m = np.concatenate([p[0] for p in parts], axis=0)
+            l = np.concatenate([p[1] for p in parts], axis=0)
+            o = np.concatenate([p[2] for p in parts], axis=0)
+            out[b] = merge_partials(m, l, o)
+    return out

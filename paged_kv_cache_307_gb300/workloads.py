@@ -262,8 +262,14 @@ def _shared_prefix_case(spec, n_seq, rng, gen, device, nan_fill):
         for s in slots[slots >= 0]:
             k[s // bs, s % bs] = float("nan")
             v[s // bs, s % bs] = float("nan")
+    # the sharing the generator built, as a group descriptor: sequences
+    # group_start[g] .. group_start[g+1]-1 hold the same first shared_blocks[g]
+    # table entries
+    group_start = torch.arange(0, B + 1, S_eff, dtype=torch.int32)
+    shared_blocks = torch.full((P,), pre_blocks, dtype=torch.int32)
     extra = {"prompts": P, "samples": S_eff, "prefix": prefix, "tails": tails,
-             "prompt_blocks": np.stack(prompt_blocks), "free_blocks": free_blocks}
+             "prompt_blocks": np.stack(prompt_blocks), "free_blocks": free_blocks,
+             "group_start": group_start.to(device), "shared_blocks": shared_blocks.to(device)}
     return DecodeCase(spec, scale_for(spec.D), q, k, v,
                       tables_t.to(device), torch.from_numpy(lens.astype(np.int32)).to(device),
                       key, value, torch.from_numpy(slots).to(device), extra)

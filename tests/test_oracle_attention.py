@@ -380,3 +380,164 @@ def test_varlen_round_reduces_to_decode_and_fixed_chunks():
     out2 = oracle.paged_prefill_varlen(q2, qs, k, v, tables, lens, 0.3)
     assert np.array_equal(np.delete(out2, 3, axis=0), np.delete(out, 3, axis=0))
 
+
+
+# ---------------------------------------------------------------- shared prefixes
+
+def shared_case(rng, P, S, pre_blocks, tails, bs=4, Hq=4, Hkv=2, D=8):
+    """P prompts x S samples: every sample's table starts with its prompt's
+    pre_blocks physical blocks, followed by private blocks for its tail;
+    unused slots and blocks are NaN."""
+    B = P * S
+    lens = [pre_blocks * bs + int(t) for t in tails]
+    nblk = [-(-L // bs) for L in lens]
+    NB = P * pre_blocks + sum(n - pre_blocks for n in nblk) + 3
+    k, v = rand_pool(rng, NB, bs, Hkv, D)
+    perm = rng.permutation(NB)
+    tables = np.full((B, max(nblk)), NB, dtype=np.int64)
+    off = 0
+    for p in range(P):
+        pb = perm[off:off + pre_blocks]
+        off += pre_blocks
+        for s in range(S):
+            b = p * S + s
+            tables[b, :pre_blocks] = pb
+            n = nblk[b] - pre_blocks
+            tables[b, pre_blocks:pre_blocks + n] = perm[off:off + n]
+            off += n
+            if n:
+                valid = lens[b] - (nblk[b] - 1) * bs
+                k[tables[b, nblk[b] - 1], valid:] = np.nan
+                v[tables[b, nblk[b] - 1], valid:] = np.nan
+    k[perm[off:]] = np.nan
+    v[perm[off:]] = np.nan
+    q = rng.standard_normal((B, Hq, D))
+    gs = np.arange(0, B + 1, S)
+    return q, k, v, tables, np.array(lens), gs, np.full(P, pre_blocks)
+
+
+def _shared_pins_pass(decode_shared=None):
+    """The shared-prefix pins, run against a given implementation."""
+    f = decode_shared or A.paged_decode_shared_prefix
+    rng = np.random.default_rng(41)
+    ok = True
+    # real sharing: equals the plain decode (and brute force for one member)
+    q, k, v, t, L, gs, sb = shared_case(rng, 3, 4, 3, [0, 5, 1, 9, 4, 4, 0, 2, 7, 3, 6, 11])
+    got = f(q, k, v, t, L, 0.4, gs, sb)
+    ok &= bool(np.isfinite(got).all()) and np.abs(got - A.paged_decode(q, k, v, t, L, 0.4)).max() <= 1e-12
+    Kc, Vc = A.gather_context(k, v, t[5], L[5])
+    ok &= np.abs(got[5] - A.brute_force_attention(q[5], Kc, Vc, 0.4)).max() <= 1e-12
+    # a claimed prefix longer than a member's full blocks is clamped
+    L2 = L.copy()
+    L2[1] = 2 * 4 + 3                   # member 1 holds only 2 full blocks of the 3 shared
+    got = f(q, k, v, t, L2, 0.4, gs, np.array([3, 3, 3]))
+    ok &= np.abs(got - A.paged_decode(q, k, v, t, L2, 0.4)).max() <= 1e-12
+    # the shared blocks are read through the first member's row
+    t3 = t.copy()
+    t3[6, 0] = t[0, 0]                  # member 2 of prompt 1 now points elsewhere
+    want = A.paged_decode(q, k, v, t, L, 0.4)
+    got = f(q, k, v, t3, L, 0.4, gs, sb)
+    ok &= np.abs(got - want).max() <= 1e-12
+    return bool(ok)
+
+
+def test_shared_prefix_decode_pins():
+    assert _shared_pins_pass()
+
+
+def test_shared_prefix_decode_equals_plain_decode_on_many_shapes():
+    rng = np.random.default_rng(42)
+    for P, S, pre, bs, Hq, Hkv in ((1, 8, 5, 4, 8, 2), (4, 2, 1, 8, 4, 4), (2, 3, 6, 4, 6, 3)):
+        tails = rng.integers(0, 3 * bs, size=P * S)
+        q, k, v, t, L, gs, sb = shared_case(rng, P, S, pre, tails, bs=bs, Hq=Hq, Hkv=Hkv)
+        got = A.paged_decode_shared_prefix(q, k, v, t, L, 0.3, gs, sb)
+        assert np.abs(got - A.paged_decode(q, k, v, t, L, 0.3)).max() <= 1e-12
+
+
+def test_shared_prefix_groups_of_one_and_empty_contexts():
+    rng = np.random.default_rng(43)
+    q, k, v, t, L = scattered_case(rng, 4, 4, 2, 8, 4, [0, 9, 1, 16])
+    # every sequence its own group with nothing shared, including L = 0
+    gs, sb = np.arange(5), np.zeros(4, dtype=np.int64)
+    got = A.paged_decode_shared_prefix(q, k, v, t, L, 0.5, gs, sb)
+    np.testing.assert_allclose(got, A.paged_decode(q, k, v, t, L, 0.5), rtol=0, atol=1e-12)
+    assert np.array_equal(got[0], np.zeros_like(got[0]))
+
+
+def test_invalid_group_descriptor_is_ignored():
+    rng = np.random.default_rng(44)
+    q, k, v, t, L, gs, sb = shared_case(rng, 2, 2, 2, [1, 2, 3, 4])
+    want = A.paged_decode(q, k, v, t, L, 0.5)
+    for bad in ([0, 2, 3], [1, 2, 4], [0, 3, 2, 4]):
+        got = A.paged_decode_shared_prefix(q, k, v, t, L, 0.5, np.array(bad), np.full(len(bad) - 1, 2))
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_shared_prefix_groups_are_found_from_the_tables():
+    rng = np.random.default_rng(45)
+    q, k, v, t, L, gs, sb = shared_case(rng, 3, 4, 3, [2, 0, 5, 1, 4, 4, 3, 2, 7, 3, 6, 1])
+    g2, s2 = A.shared_prefix_groups(t, L, 4)
+    assert np.array_equal(g2, gs) and np.array_equal(s2, sb)
+    # brute force: the longest run of leading entries common to every pair of members
+    for g in range(len(g2) - 1):
+        rows = range(g2[g], g2[g + 1])
+        n = min(min(int(L[b]) // 4 for b in rows),
+                min(next((j for j in range(t.shape[1]) if t[a, j] != t[b, j]), t.shape[1])
+                    for a in rows for b in rows))
+        assert s2[g] == n
+    # a sample that has copied its first block on write leaves the group
+    t2 = t.copy()
+    t2[4, 0] = k.shape[0] - 1
+    g3, s3 = A.shared_prefix_groups(t2, L, 4)
+    assert list(g3) == [0, 4, 5, 8, 12] and list(s3) == [3, 0, 3, 3]
+    # a divergent second block shortens the group's shared run
+    t2 = t.copy()
+    t2[9, 1] = k.shape[0] - 2
+    g4, s4 = A.shared_prefix_groups(t2, L, 4)
+    assert list(g4) == list(gs) and list(s4) == [3, 3, 1]
+
+
+def test_planted_shared_prefix_mistakes_are_caught():
+    def unweighted_merge(q, k, v, t, L, scale, gs, sb):
+        out = np.zeros(q.shape)
+        bs = k.shape[1]
+        for g in range(len(gs) - 1):
+            s0, s1 = int(gs[g]), int(gs[g + 1])
+            S = min([int(sb[g])] + [int(L[b]) // bs for b in range(s0, s1)])
+            Ks, Vs = A.gather_context(k, v, t[s0], S * bs)
+            for b in range(s0, s1):
+                Kf, Vf = A.gather_context(k, v, t[b], int(L[b]))
+                m1, l1, o1 = A.decode_partials(q[b], Ks, Vs, scale, S * bs)
+                if int(L[b]) > S * bs:
+                    m2, l2, o2 = A.decode_partials(q[b], Kf[S * bs:], Vf[S * bs:], scale, int(L[b]) - S * bs)
+                    out[b] = (o1[0] + o2[0]) / (l1[0] + l2[0])[:, None]
+                else:
+                    out[b] = o1[0] / l1[0][:, None]
+        return out
+
+    def tail_one_block_late(q, k, v, t, L, scale, gs, sb):
+        L = np.asarray(L)
+        out = A.paged_decode_shared_prefix(q, k, v, t, L, scale, gs, sb)
+        bs = k.shape[1]
+        for g in range(len(gs) - 1):
+            s0, s1 = int(gs[g]), int(gs[g + 1])
+            S = min([int(sb[g])] + [int(L[b]) // bs for b in range(s0, s1)])
+            Ks, Vs = A.gather_context(k, v, t[s0], S * bs)
+            for b in range(s0, s1):
+                Kf, Vf = A.gather_context(k, v, t[b], int(L[b]))
+                keep = np.concatenate([Ks, Kf[(S + 1) * bs:]]), np.concatenate([Vs, Vf[(S + 1) * bs:]])
+                out[b] = A.dense_attention(q[b], keep[0], keep[1], scale)
+        return out
+
+    def leaders_query(q, k, v, t, L, scale, gs, sb):
+        q2 = q.copy()
+        for g in range(len(gs) - 1):
+            q2[int(gs[g]):int(gs[g + 1])] = q[int(gs[g])]
+        return A.paged_decode_shared_prefix(q2, k, v, t, L, scale, gs, sb)
+
+    def members_own_rows(q, k, v, t, L, scale, gs, sb):   # never reads through the first member's row
+        return A.paged_decode(q, k, v, t, L, scale)
+
+    assert _shared_pins_pass()
+    for bad in (unweighted_merge, tail_one_block_late, leaders_query, members_own_rows):
+        assert not _shared_pins_pass(bad), bad.__name__

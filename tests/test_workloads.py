@@ -59,6 +59,14 @@ def test_c5_shares_prompt_blocks_eight_ways():
     assert (c.context_lens.numpy() >= c.extra["prefix"]).all()
 
 
+def test_c5_group_descriptor_is_the_sharing_the_tables_hold():
+    for small in (True, False):
+        c = W.decode_case("c5", small=small, nan_fill=False)
+        gs, sb = oracle.shared_prefix_groups(c.block_tables.numpy(), c.context_lens.numpy(), c.spec.bs)
+        assert np.array_equal(gs, c.extra["group_start"].numpy())
+        assert np.array_equal(sb, c.extra["shared_blocks"].numpy())
+
+
 def test_cow_pairs_follow_the_block_manager():
     cc = W.cow_case(small=True)
     P, S = len(cc["prompt_len"]), cc["samples"]
