@@ -51,7 +51,8 @@ WORKLOAD_TEXT = {
     "mixed": "one mixed round in one launch (pa_prefill_varlen): 8 prompts each running a 512-token prefill "
              "chunk at the end of a 1024-token context + 256 decode requests over contexts U[128,2048]; "
              "bf16 GQA 32/8, head_dim 128, block_size 16",
-    "c5": "bf16 GQA decode 32/8, 64 prompts x 8 samples sharing 1024-token prompts + private tails U[0,256]; "
+    "c5": "bf16 GQA decode 32/8, 64 prompts x 8 samples sharing 1024-token prompts + private tails U[0,256] "
+          "(pa_decode_shared: each shared block read once per prompt; GB/s counts each physical block once); "
           "plus reshape_and_cache of the new tokens",
 }
 
@@ -66,6 +67,8 @@ def parse():
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-share", action="store_true",
+                    help="c5: run plain pa_decode instead of the shared-prefix path")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -105,19 +108,25 @@ def kernel_hash(paths):
     return h.hexdigest()
 
 
-DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_307_gb300", "csrc", f)
-                  for f in ("pa_decode_kernel.cuh", "pa_decode.cu")]
+def _csrc(*names):
+    return [os.path.join(ROOT, "paged_kv_cache_307_gb300", "csrc", f) for f in names]
 
 
-def traffic_record(workload):
+DECODE_SOURCES = _csrc("pa_decode_kernel.cuh", "pa_decode.cu")
+FP8_SOURCES = _csrc("pa_decode_kernel.cuh", "pa_decode.cu", "pa_decode_fp8.cu")
+SHARED_SOURCES = _csrc("pa_decode_shared.cu", "pa_mma.cuh")
+
+
+def traffic_record(workload, sources=DECODE_SOURCES):
     """ncu DRAM bytes per launch of the decode kernel, from a committed
-    profile summary; None if it is missing or the kernel changed since."""
+    profile summary (scaled to the bench's launch as the summary states);
+    None if it is missing or the kernel changed since."""
     p = os.path.join(ROOT, "profiles", "decode_%s_traffic.json" % workload)
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    h = kernel_hash(DECODE_SOURCES)
+    h = kernel_hash(sources)
     return d.get("traffic_bytes_per_launch") if d.get("kernel_sha256") == h else None
 
 
@@ -824,13 +833,22 @@ def run_ours(args, rank, world, local_rank):
         case = W.fp8_case(case)
         k_scale, v_scale = case.extra["k_scale"], case.extra["v_scale"]
     Bsz, Hq, D = case.q.shape
-    ws = pa.alloc_workspace(case.q, case.k_cache, case.block_tables, args.partition)
+    # workloads whose samples share prompt blocks run the shared-prefix call
+    shared = "group_start" in case.extra and not fp8 and not args.no_share
+    if shared:
+        gs, sb = case.extra["group_start"], case.extra["shared_blocks"]
+        ws = pa.alloc_shared_workspace(case.q, case.k_cache, case.block_tables, sb.shape[0], args.partition)
+    else:
+        ws = pa.alloc_workspace(case.q, case.k_cache, case.block_tables, args.partition)
     out = torch.empty_like(case.q)
     stream = torch.cuda.current_stream()
     P = pa.partition_size(Bsz, Hq, spec.Hkv, D, case.max_blocks, spec.bs, args.partition, fp8=fp8)
-    launches_per_step = 2 + (1 if case.max_blocks * spec.bs > P else 0)
+    launches_per_step = 3 if shared else 2 + (1 if case.max_blocks * spec.bs > P else 0)
 
-    dec_bytes = W.algorithmic_decode_bytes(case)
+    # HBM bytes a decode call must move: each physical block once (shared
+    # prompt blocks count once; for private blocks this is the logical count)
+    logical_bytes = W.algorithmic_decode_bytes(case)
+    dec_bytes = W.unique_decode_bytes(case)
     app_bytes = W.append_bytes(case)
     step_bytes = dec_bytes + app_bytes
 
@@ -850,6 +868,9 @@ def run_ours(args, rank, world, local_rank):
         if fp8:
             pa.decode_fp8(out, q, case.k_cache, case.v_cache, k_scale, v_scale, tables, lens, case.scale,
                           partition_size=args.partition, workspace=ws)
+        elif shared:
+            pa.decode_shared(out, q, case.k_cache, case.v_cache, tables, lens, gs, sb, case.scale,
+                             partition_size=args.partition, workspace=ws)
         else:
             pa.decode(out, q, case.k_cache, case.v_cache, tables, lens, case.scale,
                       partition_size=args.partition, workspace=ws)
@@ -924,6 +945,8 @@ def run_ours(args, rank, world, local_rank):
     # back every step, overlapped with the neighbouring steps' compute)
     host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "key", "value", "slot_mapping",
                                                              "block_tables", "context_lens")}
+    if shared:
+        host["group_start"], host["shared_blocks"] = gs.cpu().pin_memory(), sb.cpu().pin_memory()
 
     def e2e_compute(d, o):
         if fp8:
@@ -931,6 +954,11 @@ def run_ours(args, rank, world, local_rank):
                                      k_scale, v_scale)
             pa.decode_fp8(o, d["q"], case.k_cache, case.v_cache, k_scale, v_scale, d["block_tables"],
                           d["context_lens"], case.scale, partition_size=args.partition, workspace=ws)
+        elif shared:
+            pa.reshape_and_cache(d["key"], d["value"], d["slot_mapping"], case.k_cache, case.v_cache)
+            pa.decode_shared(o, d["q"], case.k_cache, case.v_cache, d["block_tables"], d["context_lens"],
+                             d["group_start"], d["shared_blocks"], case.scale, partition_size=args.partition,
+                             workspace=ws)
         else:
             pa.reshape_and_cache(d["key"], d["value"], d["slot_mapping"], case.k_cache, case.v_cache)
             pa.decode(o, d["q"], case.k_cache, case.v_cache, d["block_tables"], d["context_lens"], case.scale,
@@ -949,7 +977,9 @@ def run_ours(args, rank, world, local_rank):
         return
     peak, peak_src = peaks()
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    traffic = traffic_record(args.workload)
+    traffic = traffic_record(args.workload, SHARED_SOURCES if shared else FP8_SOURCES if fp8 else DECODE_SOURCES)
+    kname = ("pa_decode_shared (shared_decode_kernel + shared_merge_kernel)" if shared else
+             "pa_decode_fp8 (decode_kernel + merge_kernel)" if fp8 else "pa_decode (decode_kernel + merge_kernel)")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
@@ -963,12 +993,17 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (K/V pool %.2f GB vs 129 MB L2); no flush"
                          % (2 * case.k_cache.numel() * case.k_cache.element_size() / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "step_bytes": step_bytes, "decode_bytes": dec_bytes, "append_bytes": app_bytes},
+                   "step_bytes": step_bytes, "decode_bytes": dec_bytes, "append_bytes": app_bytes,
+                   "decode_logical_bytes": logical_bytes,
+                   "shared_prefix": bool(shared)},
         "seq_steps_per_s": round(world * Bsz / step_s, 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
+        "logical_gbs": round(logical_bytes / (dec_ms / 1e3) / 1e9, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode (decode_kernel + merge_kernel), %.4f ms per call" % dec_ms,
+                     "bytes_per_launch": dec_bytes,
+                     "traffic_over_bytes": round(traffic / dec_bytes, 4) if traffic else None,
+                     "kernel": "%s, %.4f ms per call" % (kname, dec_ms),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

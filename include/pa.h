@@ -79,6 +79,8 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 #define PA_DEV_BAD_SLOT   2u  /* slot_mapping entry >= num_blocks * block_size */
 #define PA_DEV_BAD_LEN    4u  /* context length < 0 or > max_blocks_per_seq * block_size */
 #define PA_DEV_TIMEOUT    8u  /* a shared-memory pipeline wait exceeded its time limit */
+#define PA_DEV_BAD_GROUP 16u  /* pa_decode_shared: a group descriptor that does not cover the batch,
+                                or a member whose row does not hold its group's shared blocks */
 
 /*
  * KV append ("reshape_and_cache").  [KVS] §19.2.3: a new token's key and
@@ -145,6 +147,64 @@ int pa_decode(void* out, const void* query,
               int block_size, int num_blocks, float scale, int partition_size,
               void* workspace, size_t workspace_bytes,
               pa_dtype dtype, void* stream);
+
+/*
+ * Paged decode attention for sequences that share prompt blocks.  [KVS]
+ * §19.2.2 (Fig 19-8) and §19.2.5, [OS] §四: samples drawn from one prompt
+ * (parallel sampling, beam search, a common system prompt) point their
+ * block tables at the same physical blocks for the prompt, shared by
+ * reference count.  The result is that of pa_decode on the same arguments;
+ * the shared blocks' keys and values are read from memory once per group
+ * for all of its members' query heads (one dense tensor-core product per
+ * (shared block, KV head)) instead of once per member.
+ *
+ *   group_start    [num_groups + 1] int32, device: group g is sequences
+ *                  group_start[g] .. group_start[g+1]-1 (non-decreasing,
+ *                  from 0 to num_seqs; a sequence alone is a group of one)
+ *   shared_blocks  [num_groups] int32, device: the number of leading
+ *                  block-table entries every member of group g holds in
+ *                  common.  The shared part used is
+ *                    S_g = min(shared_blocks[g], floor(L_b / block_size)
+ *                              over the group's members b)
+ *                  whole blocks, read through the FIRST member's table row;
+ *                  each member's tokens from S_g * block_size on are read
+ *                  through its own row.  The two attention states are
+ *                  merged by log-sum-exp (exact up to rounding: the online
+ *                  softmax is associative).
+ *   partition_size 0: automatic (256-token partitions of the shared blocks;
+ *                  the private tails as pa_decode's automatic choice);
+ *                  > 0: a multiple of block_size used for both; < 0: no
+ *                  split of either.
+ *   workspace      at least pa_decode_shared_workspace_bytes() with the same
+ *                  sizes; contents on entry do not matter
+ *   other arguments as for pa_decode
+ *
+ * Device-detected conditions (PA_DEV_BAD_GROUP): a descriptor that is not
+ * non-decreasing from 0 to num_seqs is ignored (the call computes plain
+ * decode); a member whose row differs from the first member's within the
+ * shared blocks is flagged and its shared part follows the first member's
+ * row.  PA_BF16 with head_dim 64 or 128, block_size >= 8, G =
+ * num_heads / num_kv_heads <= 8, num_seqs <= 1024 and 1 <= num_groups <=
+ * 1024 run the shared path (tensor cores, m16n8k16 bf16 products with fp32
+ * accumulation, P rounded to bf16); other arguments run pa_decode unchanged
+ * (same result, no sharing exploited).  Two launches: the decode kernel and
+ * a merge kernel.
+ */
+int pa_decode_shared(void* out, const void* query,
+                     const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs,
+                     const int32_t* group_start, const int32_t* shared_blocks, int num_groups,
+                     int num_heads, int num_kv_heads, int head_dim,
+                     int block_size, int num_blocks, float scale, int partition_size,
+                     void* workspace, size_t workspace_bytes,
+                     pa_dtype dtype, void* stream);
+
+/* Bytes of workspace pa_decode_shared needs for these sizes (never less than
+ * pa_decode_workspace_bytes()).  Pure host arithmetic; no CUDA call. */
+size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int block_size, int partition_size,
+                                        int num_groups);
 
 /*
  * KV append into an e4m3 pool.  The write of pa_reshape_and_cache, with each

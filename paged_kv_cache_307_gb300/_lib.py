@@ -22,7 +22,7 @@ if not os.path.exists(LIB_PATH):
 lib = ctypes.CDLL(LIB_PATH)
 
 PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
-DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT, DEV_BAD_GROUP = 1, 2, 4, 8, 16
 
 _p, _i, _f, _sz, _i64p, _i32p = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
                                  ctypes.c_void_p, ctypes.c_void_p)
@@ -33,6 +33,11 @@ lib.pa_decode.argtypes = [_p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, 
 lib.pa_decode.restype = _i
 lib.pa_decode_noalloc.argtypes = [_p, _p, _p, _p, _i32p, _i, _i32p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
 lib.pa_decode_noalloc.restype = _i
+lib.pa_decode_shared.argtypes = [_p, _p, _p, _p, _i32p, _i, _i32p, _i, _i32p, _i32p, _i, _i, _i, _i, _i, _i, _f, _i,
+                                 _p, _sz, _i, _p]
+lib.pa_decode_shared.restype = _i
+lib.pa_decode_shared_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
+lib.pa_decode_shared_workspace_bytes.restype = _sz
 lib.pa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 lib.pa_decode_workspace_bytes.restype = _sz
 lib.pa_decode_partition_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
@@ -162,6 +167,41 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, partitio
                          block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB,
                          ctypes.c_float(scale), partition_size, _ptr(workspace), workspace.numel(),
                          _dtype(q), _stream(stream)), "pa_decode")
+    return out
+
+
+def shared_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size,
+                           partition_size=0, num_groups=1):
+    return lib.pa_decode_shared_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
+                                                block_size, partition_size, num_groups)
+
+
+def alloc_shared_workspace(q, k_cache, block_tables, num_groups, partition_size=0):
+    B, Hq, D = q.shape
+    n = shared_workspace_bytes(B, Hq, k_cache.shape[2], D, block_tables.shape[1], k_cache.shape[1],
+                               partition_size, num_groups)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+
+
+def decode_shared(out, q, k_cache, v_cache, block_tables, context_lens, group_start, shared_blocks, scale,
+                  partition_size=0, workspace=None, stream=None):
+    """out[B,Hq,D] = paged decode attention of q over the pool, reading the
+    shared prompt blocks of each group (sequences group_start[g] ..
+    group_start[g+1]-1 share their first shared_blocks[g] table entries)
+    once for the whole group."""
+    _contig(out, q, k_cache, v_cache, block_tables, context_lens, group_start, shared_blocks)
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert group_start.dtype == torch.int32 and shared_blocks.dtype == torch.int32
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    ng = shared_blocks.shape[0]
+    assert group_start.shape[0] == ng + 1
+    if workspace is None:
+        workspace = alloc_shared_workspace(q, k_cache, block_tables, ng, partition_size)
+    _check(lib.pa_decode_shared(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(context_lens), B, _ptr(group_start),
+                                _ptr(shared_blocks), ng, Hq, Hkv, D, bs, NB, ctypes.c_float(scale), partition_size,
+                                _ptr(workspace), workspace.numel(), _dtype(q), _stream(stream)), "pa_decode_shared")
     return out
 
 

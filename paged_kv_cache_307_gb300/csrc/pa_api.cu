@@ -91,7 +91,8 @@ bool encode_map(CUtensorMap* map, const void* base, pa_dtype dt, int rank, const
 extern "C" int pa_last_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   const unsigned a = pa::fetch_status_cache_ops();
-  const unsigned b = pa::fetch_status_decode() | pa::fetch_status_decode_fp8();
+  const unsigned b0 = pa::fetch_status_decode(), b1 = pa::fetch_status_decode_fp8(), b2 = pa::fetch_status_shared();
+  const unsigned b = (b0 == 0xffffffffu || b1 == 0xffffffffu || b2 == 0xffffffffu) ? 0xffffffffu : (b0 | b1 | b2);
   const unsigned c = pa::fetch_status_prefill();
   const unsigned d = pa::fetch_status_selftest();
   if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu || d == 0xffffffffu) return PA_ERR_CUDA;
@@ -111,6 +112,7 @@ extern "C" const char* pa_strerror(int code) {
     case (int)PA_DEV_BAD_SLOT: return "device: slot outside the pool";
     case (int)PA_DEV_BAD_LEN: return "device: context length outside its block-table row";
     case (int)PA_DEV_TIMEOUT: return "device: pipeline wait timed out";
+    case (int)PA_DEV_BAD_GROUP: return "device: shared-prefix group descriptor inconsistent with the block tables";
     default: return code > 0 ? "device: several conditions (bitmask)" : "unknown error";
   }
 }

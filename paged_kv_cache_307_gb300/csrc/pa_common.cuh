@@ -229,6 +229,7 @@ bool raise_smem_limit(const void* kernel, int dev);
 unsigned fetch_status_cache_ops();
 unsigned fetch_status_decode();
 unsigned fetch_status_decode_fp8();
+unsigned fetch_status_shared();
 unsigned fetch_status_prefill();
 unsigned fetch_status_selftest();
 

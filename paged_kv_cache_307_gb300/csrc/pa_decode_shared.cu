@@ -1,0 +1,864 @@
+// pa_decode_shared.cu — paged decode attention for batches whose sequences
+// share prompt blocks (pa_decode_shared).
+//
+// What it computes: the result of pa_decode.  Samples drawn from one prompt
+// (parallel sampling, beam search, a common system prompt) point their block
+// tables at the same physical blocks for the prompt, each block carrying a
+// reference count ("19.2 KV Cache 系统化管理" §19.2.2 Fig 19-8 and §19.2.5;
+// "LLM 推理引擎的内存管理与调度…" §四).  The caller names those groups: the
+// sequences group_start[g] .. group_start[g+1]-1 hold the same first
+// shared_blocks[g] block-table entries.  Attention over the shared tokens is
+// then one dense product for the whole group: every query row of every
+// member reads the same K/V rows.  The online softmax of §19.2.3 is
+// associative, so each member's result is the log-sum-exp combination of
+// its state over the shared blocks and its state over its own tail.
+//
+// How (GB300):
+//  * Work item = either a SHARED item (group, partition of the shared
+//    blocks, KV heads, row chunk) whose rows are (member, query head) pairs
+//    of the group, or a TAIL item (sequence, partition of its own tokens
+//    after the shared blocks, four KV heads) whose rows are the sequence's
+//    query heads.  A shared block is read from HBM once for every row of the
+//    group instead of once per member.
+//  * Items are enumerated densely per CTA (a persistent grid strides over
+//    them): every CTA builds, in shared memory, the clamped lengths, the
+//    per-group shared length S_g = min(shared_blocks[g], floor(L_b / bs)
+//    over the members) and prefix sums of items per group and of tail items
+//    per sequence; a group's shared items come first, then its members'
+//    tails, so CTAs running side by side mix the tensor-core-heavy shared
+//    items with the streaming tail items.
+//  * One producer warp per CTA fills a ring of stages by TMA; a stage holds
+//    four (block, KV head) tiles of K and V (128-byte-swizzled 64-column
+//    spans): four heads of one block, or two heads of two blocks.
+//  * Four consumer warps run tensor-core products with the block's tokens as
+//    the M rows (S^T = K Q^T, m16n8k16, then O^T = V^T P with P^T
+//    transposed in registers by movmatrix): each warp owns 8 or 16 query
+//    rows (one or two n-tiles) of one KV head.  Groups of up to 16 rows per
+//    head: one warp per head, four heads per stage.  Groups of 17..32 rows:
+//    two warps per head (16 rows each), two heads of two blocks per stage.
+//    Larger groups are split into chunks of 32 rows.  Tails: one warp per
+//    head, the sequence's G query heads as the columns.
+//  * A warp owns whole rows over all of an item's tokens, so no merge
+//    between warps.  A row whose sequence has one partition in all writes
+//    its normalised output; otherwise it writes (max, sum, unnormalised
+//    output) to its partition's slot of the workspace and a merge kernel
+//    combines the slots.
+//  * Waits are bounded (2 s) as in pa_decode: a wait that runs out sets
+//    PA_DEV_TIMEOUT, the CTA skips its remaining work and waits (bounded) for
+//    its own TMA loads before it exits.
+#include "pa_common.cuh"
+#include "pa_mma.cuh"
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_status_shared;
+
+constexpr int kSW = 4;                       // consumer warps
+constexpr int kST = (kSW + 1) * 32;          // threads per CTA
+constexpr int kTiles = 4;                    // (block, KV head) tiles per stage
+constexpr int kSMaxSeqs = 1024;              // sequences per call on this path
+constexpr int kSMaxGroups = 1024;            // groups per call on this path
+constexpr float kLog2eS = 1.4426950408889634f;
+constexpr uint32_t kAlign = 1024;
+
+struct SParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* group_start;
+  const int32_t* shared_blocks;
+  float* ws_ml;                 // [B*Hq*max_parts][2]  (m in log2 units, l)
+  float* ws_o;                  // [B*Hq*max_parts][D]
+  int32_t* ws_parts;            // [B] partitions of each sequence (shared + tail)
+  int B, Hq, Hkv, G, ng;
+  int max_blocks, bs, num_blocks;
+  int ps_blocks;                // shared partition, blocks
+  int pt_tokens;                // tail partition, tokens (a multiple of bs)
+  int max_parts;
+  int nstage;
+  uint32_t tile_bytes;          // one (block, head) tile of K (or V): bs * D * 2
+  float qscale;                 // scale * log2(e)
+};
+
+// Shared-memory tables every CTA builds (ngE = effective number of groups).
+struct Tables {
+  int* Ls;      // [B]      clamped context lengths
+  int* preT;    // [B+1]    prefix of tail items per sequence
+  int* preG;    // [ngE+1]  prefix of items per group (shared + tails)
+  int* shc;     // [ngE]    shared items per group
+  int* Sg;      // [ngE]    shared blocks used per group
+  int* gsm;     // [ngE+1]  group boundaries
+  int ngE;
+};
+
+struct SItem {
+  int s0;          // first sequence of the rows (the group's first member / the tail's sequence)
+  int R;           // rows of this item (<= 32)
+  int row0;        // first row of this chunk within the group's rows
+  int kvh0;        // first KV head
+  int bps;         // blocks per stage (1 or 2); heads per stage = 4 / bps
+  int nt;          // n-tiles (8 rows each) per warp
+  int wh;          // warps per head
+  int jb, je, t1;  // blocks [jb, je) of row s0's table; tokens end at t1
+  int slot;        // partition slot of this item in each row's sequence
+  int shared;      // 1: shared item
+  int S;           // the group's shared blocks
+  int s1;          // end of the group's sequences (shared items)
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Partitions of sequence b: shared ones (if its group shares) then tail
+// ones; a sequence with nothing to read still has one (it writes zeros).
+__device__ __forceinline__ void seq_parts(const SParams& p, int S, int L, int& nsp, int& ntp) {
+  nsp = S > 0 ? ceil_div(S, p.ps_blocks) : 0;
+  const int tail = L - S * p.bs;
+  ntp = tail > 0 ? ceil_div(tail, p.pt_tokens) : (nsp == 0 ? 1 : 0);
+}
+
+// Items of one shared partition of a group with R rows per KV head.
+__device__ __forceinline__ int shared_items_per_part(const SParams& p, int R) {
+  if (R <= 16) return ceil_div(p.Hkv, 4);
+  return ceil_div(R, 32) * ceil_div(p.Hkv, 2);
+}
+
+// Block-wide exclusive scan of arr[0..n) in place; arr[n] = total.
+__device__ void block_scan(int* arr, int n, int* wsum) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = (n + kST - 1) / kST;
+  const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
+  int sum = 0;
+  for (int i = i0; i < i1; ++i) sum += arr[i];
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+  for (int i = i0; i < i1; ++i) {
+    const int c = arr[i];
+    arr[i] = run;
+    run += c;
+  }
+  if (threadIdx.x == kST - 1) arr[n] = run;
+  __syncthreads();
+}
+
+// Item i -> its description (every role computes the same).
+__device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i, SItem& it) {
+  int lo = 0, hi = t.ngE - 1;           // last group whose first item is <= i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.preG[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
+  const int r = i - t.preG[g];
+  const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
+  const int S = t.Sg[g];
+  it.S = S;
+  if (r < t.shc[g]) {
+    const int R = (s1 - s0) * p.G;
+    int nhg, chunks;
+    if (R <= 16) {
+      it.nt = R <= 8 ? 1 : 2;
+      it.wh = 1;
+      it.bps = 1;
+      nhg = ceil_div(p.Hkv, 4);
+      chunks = 1;
+    } else {
+      it.nt = 2;
+      it.wh = 2;
+      it.bps = 2;
+      nhg = ceil_div(p.Hkv, 2);
+      chunks = ceil_div(R, 32);
+    }
+    const int per = nhg * chunks;
+    const int part = r / per, k = r - part * per;
+    const int chunk = k / nhg;
+    it.kvh0 = (k - chunk * nhg) * (4 / it.bps);
+    it.row0 = chunk * 32;
+    it.R = min(32, R - it.row0);
+    it.s0 = s0;
+    it.jb = part * p.ps_blocks;
+    it.je = min(S, it.jb + p.ps_blocks);
+    it.t1 = it.je * p.bs;
+    it.slot = part;
+    it.shared = 1;
+    it.s1 = s1;
+  } else {
+    const int r2 = r - t.shc[g] + t.preT[s0];
+    int blo = s0, bhi = s1 - 1;         // last member whose first tail item is <= r2
+    while (blo < bhi) {
+      const int mid = (blo + bhi + 1) >> 1;
+      if (t.preT[mid] <= r2) blo = mid;
+      else bhi = mid - 1;
+    }
+    const int b = blo;
+    const int rr = r2 - t.preT[b];
+    const int nhg = ceil_div(p.Hkv, 4);
+    const int part = rr / nhg;
+    it.kvh0 = (rr - part * nhg) * 4;
+    const int T0 = S * p.bs + part * p.pt_tokens;
+    const int L = t.Ls[b];
+    it.t1 = max(T0, min(L, T0 + p.pt_tokens));
+    it.jb = T0 / p.bs;
+    it.je = ceil_div(it.t1, p.bs);
+    int nsp, ntp;
+    seq_parts(p, S, L, nsp, ntp);
+    it.slot = nsp + part;
+    it.s0 = b;
+    it.R = p.G;
+    it.row0 = 0;
+    it.nt = 1;
+    it.wh = 1;
+    it.bps = 1;
+    it.shared = 0;
+    it.s1 = b + 1;
+  }
+}
+
+// One consumer warp's share of an item: NT n-tiles (8 query rows each) of
+// KV head kvh0 + hd over the tiles hd*bps .. hd*bps+bps-1 of every stage.
+template <int D, int NT>
+__device__ __forceinline__ void run_rows(const SParams& p, const Tables& t, const SItem& it, int hd, int rbase,
+                                         bool active, unsigned char* tilesK, unsigned char* tilesV,
+                                         uint64_t* full, uint64_t* empty, volatile int* abort_flag,
+                                         int& st_idx, uint32_t& st_ph) {
+  constexpr int KS = D / 16;     // k-steps of S^T
+  constexpr int MT = D / 16;     // M tiles of O^T
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int kvh = it.kvh0 + hd;
+
+  // this lane's Q^T column g of each n-tile: row rbase + 8n + g
+  uint32_t qb[NT][KS][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int rho = rbase + 8 * n + g;
+    const bool ok = active && rho < it.R;
+    const int gr = it.row0 + rho;
+    const int seq = it.s0 + (ok ? gr / p.G : 0);
+    const int qh = kvh * p.G + (ok ? gr % p.G : 0);
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        static_cast<const unsigned char*>(p.q) + ((size_t)seq * p.Hq + (ok ? qh : 0)) * (D * 2));
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      qb[n][kk][0] = ok ? __ldg(qp + kk * 8 + tq) : 0u;
+      qb[n][kk][1] = ok ? __ldg(qp + kk * 8 + 4 + tq) : 0u;
+    }
+  }
+  float OT[MT][NT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) OT[m][n][0] = OT[m][n][1] = OT[m][n][2] = OT[m][n][3] = 0.f;
+  float mh[NT][2], lh[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) mh[n][0] = mh[n][1] = -INFINITY, lh[n][0] = lh[n][1] = 0.f;
+  const uint32_t half_bytes = (uint32_t)p.bs * 128u;
+
+  const int nstages = ceil_div(it.je - it.jb, it.bps);
+  for (int s = 0; s < nstages; ++s) {
+    const int st = st_idx;
+    const uint32_t ph = st_ph;
+    if (++st_idx == p.nstage) {
+      st_idx = 0;
+      st_ph ^= 1u;
+    }
+    bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+    if (live) {
+      const bool late = !mbar_wait(&full[st], ph);
+      if (__any_sync(0xffffffffu, late)) {
+        live = false;
+        if (lane == 0) {
+          atomicOr(&g_status_shared, PA_DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+    }
+    if (live && active) {
+#pragma unroll 1
+      for (int kb = 0; kb < it.bps; ++kb) {
+        const int j = it.jb + s * it.bps + kb;
+        if (j >= it.je) break;
+        const int valid = min(p.bs, it.t1 - j * p.bs);
+        const int tile = st * kTiles + hd * it.bps + kb;
+        unsigned char* vt_ptr = tilesV + (size_t)tile * p.tile_bytes;
+        const uint32_t kt = smem_u32(tilesK + (size_t)tile * p.tile_bytes);
+        const uint32_t vt = smem_u32(vt_ptr);
+        if (valid < p.bs) {
+          // slots past the context may hold anything; P is 0 there, but
+          // 0 * NaN is NaN inside the product, so clear those V rows.  Only
+          // tail tiles can be partial, and each of those has one reader.
+          for (int idx = lane; idx < (p.bs - valid) * (D / 8); idx += 32) {
+            const int tk = valid + idx / (D / 8), c = idx % (D / 8);
+            *reinterpret_cast<uint4*>(vt_ptr + (c >> 3) * half_bytes + tk * 128 + (c & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        for (int tb = 0; tb < valid; tb += 16) {
+          float St[NT][4];
+#pragma unroll
+          for (int n = 0; n < NT; ++n) St[n][0] = St[n][1] = St[n][2] = St[n][3] = 0.f;
+          {
+            // K rows as the A fragment: lanes 0-7 tokens tb..+7, chunk 2kk;
+            // 8-15 tokens tb+8..+15, chunk 2kk; 16-31 the same for chunk 2kk+1
+            const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              const int c = 2 * kk + (lane >> 4);
+              uint32_t a[4];
+              ldsm_x4(kt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+              for (int n = 0; n < NT; ++n) mma_bf16_16816(St[n], a, qb[n][kk][0], qb[n][kk][1]);
+            }
+          }
+          const bool ok0 = tb + g < valid, ok1 = tb + g + 8 < valid;
+          uint32_t pb[NT][2];
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            St[n][0] = ok0 ? St[n][0] * p.qscale : -INFINITY;
+            St[n][1] = ok0 ? St[n][1] * p.qscale : -INFINITY;
+            St[n][2] = ok1 ? St[n][2] * p.qscale : -INFINITY;
+            St[n][3] = ok1 ? St[n][3] * p.qscale : -INFINITY;
+            float alpha[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(St[n][e], St[n][2 + e]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float mn = fmaxf(mh[n][e], mx);
+              alpha[e] = mn == -INFINITY ? 1.f : exp2f(mh[n][e] - mn);
+              mh[n][e] = mn;
+              lh[n][e] *= alpha[e];
+            }
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                OT[m][n][0] *= alpha[0];
+                OT[m][n][1] *= alpha[1];
+                OT[m][n][2] *= alpha[0];
+                OT[m][n][3] *= alpha[1];
+              }
+            }
+            float pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pw[e] = St[n][e] == -INFINITY ? 0.f : exp2f(St[n][e] - mh[n][e & 1]);
+              lh[n][e & 1] += pw[e];
+            }
+            pb[n][0] = movmatrix_t(pack_bf16(pw[0], pw[1]));   // tokens 0-7
+            pb[n][1] = movmatrix_t(pack_bf16(pw[2], pw[3]));   // tokens 8-15
+          }
+          {
+            // V^T as the A fragment (ldmatrix.trans): lanes 0-7 tokens tb..+7
+            // chunk 2m; 8-15 the same tokens, chunk 2m+1; 16-31 tokens
+            // tb+8..+15, chunks 2m, 2m+1
+            const int tt = min(tb + (lane & 7) + ((lane >> 4) << 3), p.bs - 1);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const int c = 2 * m + ((lane >> 3) & 1);
+              uint32_t a[4];
+              ldsm_x4_t(vt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), a[0], a[1], a[2],
+                        a[3]);
+#pragma unroll
+              for (int n = 0; n < NT; ++n) mma_bf16_16816(OT[m][n], a, pb[n][0], pb[n][1]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+  if (!active) return;
+
+  // the column sums are split over the 8 lanes sharing tq
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      lh[n][e] += __shfl_xor_sync(0xffffffffu, lh[n][e], 4);
+      lh[n][e] += __shfl_xor_sync(0xffffffffu, lh[n][e], 8);
+      lh[n][e] += __shfl_xor_sync(0xffffffffu, lh[n][e], 16);
+    }
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int rho = rbase + 8 * n + 2 * tq + e;
+      if (rho >= it.R) continue;
+      const int gr = it.row0 + rho;
+      const int seq = it.s0 + gr / p.G;
+      const int qh = kvh * p.G + gr % p.G;
+      int nsp, ntp;
+      seq_parts(p, it.S, t.Ls[seq], nsp, ntp);
+      const size_t bh = (size_t)seq * p.Hq + qh;
+      if (nsp + ntp == 1) {
+        const float inv = lh[n][e] > 0.f ? 1.f / lh[n][e] : 0.f;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + bh * D;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          o[16 * m + g] = __float2bfloat16_rn(OT[m][n][e] * inv);
+          o[16 * m + 8 + g] = __float2bfloat16_rn(OT[m][n][2 + e] * inv);
+        }
+      } else {
+        const size_t slot = bh * p.max_parts + it.slot;
+        float* o = p.ws_o + slot * D;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          o[16 * m + g] = OT[m][n][e];
+          o[16 * m + 8 + g] = OT[m][n][2 + e];
+        }
+        if (g == 0) {
+          p.ws_ml[slot * 2] = mh[n][e];
+          p.ws_ml[slot * 2 + 1] = lh[n][e];
+        }
+      }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kST, 2)
+shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                     const SParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1))) & (kAlign - 1));
+  const uint32_t stage_bytes = kTiles * p.tile_bytes;
+  unsigned char* tilesK = smem;
+  unsigned char* tilesV = smem + (size_t)p.nstage * stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(tilesV + (size_t)p.nstage * stage_bytes);
+  uint64_t* empty = full + p.nstage;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.nstage);
+  int* wsum = const_cast<int*>(abort_flag) + 4;      // [8]
+  const int ngMax = max(p.ng, p.B);
+  Tables t;
+  t.Ls = wsum + 8;
+  t.preT = t.Ls + p.B;
+  t.gsm = t.preT + p.B + 1;
+  t.preG = t.gsm + ngMax + 1;
+  t.shc = t.preG + ngMax + 1;
+  t.Sg = t.shc + ngMax;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.nstage; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSW);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+
+  // ---- tables: clamped lengths, the group descriptor (checked), shared
+  // blocks per group, item counts, prefix sums
+  const int Lmax = p.max_blocks * p.bs;
+  for (int b = threadIdx.x; b < p.B; b += kST) {
+    int L = __ldg(&p.context_lens[b]);
+    if (L < 0 || L > Lmax) {
+      if (blockIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_LEN);
+      L = L < 0 ? 0 : Lmax;
+    }
+    t.Ls[b] = L;
+  }
+  bool ok = true;
+  for (int g = threadIdx.x; g < p.ng; g += kST) {
+    const int a = __ldg(&p.group_start[g]), c = __ldg(&p.group_start[g + 1]);
+    if (a > c || a < 0 || c > p.B) ok = false;
+  }
+  if (threadIdx.x == 0 && (__ldg(&p.group_start[0]) != 0 || __ldg(&p.group_start[p.ng]) != p.B)) ok = false;
+  const bool valid = __syncthreads_and(ok) != 0;
+  if (!valid && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_GROUP);
+  t.ngE = valid ? p.ng : p.B;
+  for (int g = threadIdx.x; g <= t.ngE; g += kST) t.gsm[g] = valid ? __ldg(&p.group_start[g]) : g;
+  __syncthreads();
+  const int ipt = ceil_div(p.Hkv, 4);        // tail items per tail partition
+  for (int g = threadIdx.x; g < t.ngE; g += kST) {
+    const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
+    int S = 0;
+    if (valid && s1 - s0 >= 2) {
+      S = min(max(__ldg(&p.shared_blocks[g]), 0), p.max_blocks);
+      for (int b = s0; b < s1; ++b) S = min(S, t.Ls[b] / p.bs);
+    }
+    t.Sg[g] = S;
+    const int nspg = S > 0 ? ceil_div(S, p.ps_blocks) : 0;
+    t.shc[g] = nspg * shared_items_per_part(p, (s1 - s0) * p.G);
+    int tsum = 0;
+    for (int b = s0; b < s1; ++b) {
+      int nsp, ntp;
+      seq_parts(p, S, t.Ls[b], nsp, ntp);
+      t.preT[b] = ntp * ipt;
+      tsum += ntp * ipt;
+      if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
+    }
+    t.preG[g] = t.shc[g] + tsum;
+  }
+  __syncthreads();
+  block_scan(t.preT, p.B, wsum);
+  block_scan(t.preG, t.ngE, wsum);
+  const int n_items = t.preG[t.ngE];
+
+  if (warp == kSW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&mapK);
+      prefetch_tensormap(&mapV);
+    }
+    const uint64_t pol = policy_evict_first();
+    constexpr int HALVES = D * 2 / 128;            // 128-byte column spans per row
+    constexpr int OPS = kTiles * 2 * HALVES;       // TMA loads per full stage
+    int st_idx = 0;
+    uint32_t st_ph = 0;
+    uint32_t ucount = 0;                           // stages walked so far
+    uint32_t armed_end = 0;                        // 1 + index of the last stage armed
+    for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+      SItem it;
+      s_item(p, t, v, it);
+      const int32_t* row = p.block_tables + (size_t)it.s0 * p.max_blocks;
+      const int nblk = it.je - it.jb;
+      const int nh = 4 / it.bps;
+      // A shared item checks that every member's row names the shared blocks
+      // it reads through the first member's row (once per group partition).
+      const bool check = it.shared && it.kvh0 == 0 && it.row0 == 0;
+      for (int j0 = 0; j0 < nblk; j0 += 32) {
+        const int n = min(32, nblk - j0);
+        int blk = 0;
+        if (lane < n) {
+          blk = __ldg(&row[it.jb + j0 + lane]);
+          if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            atomicOr(&g_status_shared, PA_DEV_BAD_BLOCK);
+            blk = 0;    // keep every copy inside the pool
+          }
+        }
+        if (check) {
+          bool same = true;
+          if (lane < n)
+            for (int b = it.s0 + 1; b < it.s1; ++b)
+              same &= __ldg(&p.block_tables[(size_t)b * p.max_blocks + it.jb + j0 + lane]) ==
+                      __ldg(&row[it.jb + j0 + lane]);
+          if (!__all_sync(0xffffffffu, same) && lane == 0) atomicOr(&g_status_shared, PA_DEV_BAD_GROUP);
+        }
+        // stages of this 32-block window: bps blocks each
+        for (int i = 0; i < n; i += it.bps) {
+          const int st = st_idx;
+          const uint32_t ph = st_ph;
+          const uint32_t u = ucount++;
+          if (++st_idx == p.nstage) {
+            st_idx = 0;
+            st_ph ^= 1u;
+          }
+          const int nb = min(it.bps, n - i);        // blocks in this stage
+          const int heads = min(nh, p.Hkv - it.kvh0);
+          int go = 0;
+          if (lane == 0 && !*abort_flag) {
+            if (!mbar_wait(&empty[st], ph ^ 1u)) {
+              atomicOr(&g_status_shared, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            } else {
+              mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * nb * heads) * p.tile_bytes);
+              go = 1;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, go, 0)) {
+            armed_end = u + 1;
+            // lane l: tile l / (2*HALVES), K (even op) or V (odd op), span
+            const int tile = lane / (2 * HALVES);
+            const int op = lane % (2 * HALVES);
+            const int kv = op & 1, hh = op >> 1;
+            const int hd = tile / it.bps, kb = tile % it.bps;
+            const int bi = __shfl_sync(0xffffffffu, blk, min(i + kb, 31));
+            if (lane < OPS && hd < heads && kb < nb) {
+              unsigned char* dst = (kv ? tilesV : tilesK) + (size_t)(st * kTiles + tile) * p.tile_bytes +
+                                   (size_t)hh * p.bs * 128;
+              tma_load_4d(dst, kv ? &mapV : &mapK, &full[st], hh * 64, it.kvh0 + hd, 0, bi, pol);
+            }
+          }
+        }
+      }
+    }
+    // Never leave the CTA with TMA writes into its shared memory in flight:
+    // wait (bounded) for the last stages armed.
+    if (lane == 0) {
+      const uint32_t first = armed_end > (uint32_t)p.nstage ? armed_end - p.nstage : 0u;
+      for (uint32_t u = first; u < armed_end; ++u)
+        mbar_wait(&full[u % p.nstage], (u / p.nstage) & 1u);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  int st_idx = 0;
+  uint32_t st_ph = 0;
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    SItem it;
+    s_item(p, t, v, it);
+    const int hd = warp / it.wh;
+    const int rbase = (warp % it.wh) * 8 * it.nt;
+    const bool active = hd < 4 / it.bps && it.kvh0 + hd < p.Hkv && rbase < it.R;
+    if (it.nt == 1)
+      run_rows<D, 1>(p, t, it, hd, rbase, active, tilesK, tilesV, full, empty, abort_flag, st_idx, st_ph);
+    else
+      run_rows<D, 2>(p, t, it, hd, rbase, active, tilesK, tilesV, full, empty, abort_flag, st_idx, st_ph);
+  }
+}
+
+// One warp per (sequence, query head) whose sequence has several partitions.
+template <int D>
+__global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
+  constexpr int PER = D / 32;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)p.B * p.Hq) return;
+  const int b = (int)(gw / p.Hq);
+  const int nparts = p.ws_parts[b];
+  if (nparts <= 1) return;
+  const size_t base = (size_t)gw * p.max_parts;
+  float M = -INFINITY;
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[(base + i) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float den = 0.f;
+  for (int i = lane; i < nparts; i += 32) {
+    const float mi = p.ws_ml[(base + i) * 2];
+    if (mi != -INFINITY) den += exp2f(mi - M) * p.ws_ml[(base + i) * 2 + 1];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  for (int i = 0; i < nparts; ++i) {
+    const float mi = p.ws_ml[(base + i) * 2];
+    const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
+    const float* oi = p.ws_o + (base + i) * D;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oi[lane + 32 * k], acc[k]);
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)gw * D;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) out[lane + 32 * k] = __float2bfloat16_rn(den > 0.f ? acc[k] / den : 0.f);
+}
+
+// ------------------------------------------------------------------ host side
+
+std::mutex g_smu;
+std::map<std::tuple<const void*, int, int, int, int, int>, CUtensorMap> g_smaps;   // (base, nb, bs, h, d, dev)
+std::map<std::tuple<const void*, int, size_t>, int> g_socc;                          // (kernel, dev, smem)
+
+bool shared_map(CUtensorMap* out, const void* base, int nb, int bs, int h, int d, int dev) {
+  const auto key = std::make_tuple(base, nb, bs, h, d, dev);
+  std::lock_guard<std::mutex> lk(g_smu);
+  auto f = g_smaps.find(key);
+  if (f != g_smaps.end()) {
+    *out = f->second;
+    return true;
+  }
+  const uint64_t dims[4] = {(uint64_t)d, (uint64_t)h, (uint64_t)bs, (uint64_t)nb};
+  const uint64_t str[3] = {(uint64_t)d * 2, (uint64_t)h * d * 2, (uint64_t)bs * h * d * 2};
+  const uint32_t box[4] = {64, 1, (uint32_t)bs, 1};   // one 128-byte row span of one head
+  if (!encode_map(out, base, PA_BF16, 4, dims, str, box, true)) return false;
+  if (g_smaps.size() > 64) g_smaps.clear();
+  g_smaps[key] = *out;
+  return true;
+}
+
+int shared_occupancy(const void* kernel, size_t smem, int dev) {
+  std::lock_guard<std::mutex> lk(g_smu);
+  const auto key = std::make_tuple(kernel, dev, smem);
+  auto f = g_socc.find(key);
+  if (f != g_socc.end()) return f->second;
+  if (!raise_smem_limit(kernel, dev)) return 0;
+  int occ = 0;
+  if (!ck(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kST, smem),
+          "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
+    return 0;
+  g_socc[key] = occ;
+  return occ;
+}
+
+// Automatic shared partition: 256 tokens (at least one block).
+constexpr int kSharedPartTokens = 256;
+
+struct SharedPlan {
+  int ps_blocks, pt_tokens, max_parts;
+  size_t ml_bytes, o_bytes, parts_bytes;
+};
+
+bool shared_eligible(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_groups,
+                     pa_dtype dtype) {
+  const int G = num_kv_heads > 0 ? num_heads / num_kv_heads : 0;
+  return dtype == PA_BF16 && (head_dim == 64 || head_dim == 128) && block_size >= 8 && G >= 1 && G <= 8 &&
+         num_seqs <= kSMaxSeqs && num_groups >= 1 && num_groups <= kSMaxGroups;
+}
+
+SharedPlan shared_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_blocks, int block_size,
+                       int partition_size) {
+  SharedPlan pl;
+  const int max_ctx = max_blocks * block_size;
+  const int G = num_heads / num_kv_heads;
+  if (partition_size < 0) {
+    pl.ps_blocks = max_blocks;
+    pl.pt_tokens = max_ctx;
+  } else if (partition_size > 0) {
+    pl.ps_blocks = partition_size / block_size;
+    pl.pt_tokens = partition_size;
+  } else {
+    pl.ps_blocks = kSharedPartTokens / block_size > 0 ? kSharedPartTokens / block_size : 1;
+    pl.pt_tokens = pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, 0);
+    (void)G;
+  }
+  if (pl.pt_tokens > max_ctx) pl.pt_tokens = max_ctx;
+  if (pl.ps_blocks > max_blocks) pl.ps_blocks = max_blocks;
+  const int minp = pl.ps_blocks * block_size < pl.pt_tokens ? pl.ps_blocks * block_size : pl.pt_tokens;
+  // a sequence has at most ceil(x / Ps) + ceil((max_ctx - x) / Pt) partitions
+  pl.max_parts = (max_ctx + minp - 1) / minp + 1;
+  const size_t rows = (size_t)num_seqs * num_heads * pl.max_parts;
+  pl.parts_bytes = ((size_t)num_seqs * 4 + 255) / 256 * 256;
+  pl.ml_bytes = (rows * 8 + 255) / 256 * 256;
+  pl.o_bytes = rows * head_dim * 4;
+  return pl;
+}
+
+}  // namespace
+
+unsigned fetch_status_shared() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_shared, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (v && cudaMemcpyToSymbol(g_status_shared, &zero, sizeof(zero)) != cudaSuccess) return 0xffffffffu;
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                                   int max_blocks_per_seq, int block_size, int partition_size,
+                                                   int num_groups) {
+  const size_t plain = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                 block_size, partition_size);
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+      max_blocks_per_seq <= 0 || !supported_block_size(block_size) ||
+      (partition_size > 0 && partition_size % block_size))
+    return plain;
+  if (!shared_eligible(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_groups, PA_BF16)) return plain;
+  const SharedPlan pl =
+      shared_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size);
+  const size_t need = pl.parts_bytes + pl.ml_bytes + pl.o_bytes;
+  return need > plain ? need : plain;
+}
+
+extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                int num_seqs, const int32_t* group_start, const int32_t* shared_blocks,
+                                int num_groups, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, float scale, int partition_size, void* workspace,
+                                size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+      !supported_head_dim(head_dim) || !supported_block_size(block_size) || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0 || num_groups < 0)
+    return PA_ERR_SHAPE;
+  if (partition_size > 0 && partition_size % block_size) return PA_ERR_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (num_groups > 0 && (!group_start || !shared_blocks)) return PA_ERR_NULL;
+  if (!shared_eligible(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_groups, dtype))
+    return pa_decode(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size, workspace,
+                     workspace_bytes, dtype, stream);
+  if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  const SharedPlan pl =
+      shared_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size);
+  const size_t need = pa_decode_shared_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                       max_blocks_per_seq, block_size, partition_size, num_groups);
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+
+  int dev = 0;
+  if (!ck(cudaGetDevice(&dev), "cudaGetDevice")) return PA_ERR_CUDA;
+  CUtensorMap mapK, mapV;
+  if (!shared_map(&mapK, k_cache, num_blocks, block_size, num_kv_heads, head_dim, dev) ||
+      !shared_map(&mapV, v_cache, num_blocks, block_size, num_kv_heads, head_dim, dev)) {
+    note_host_error("cuTensorMapEncodeTiled failed for the K/V pool");
+    return PA_ERR_CUDA;
+  }
+
+  SParams prm;
+  prm.out = out;
+  prm.q = query;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.group_start = group_start;
+  prm.shared_blocks = shared_blocks;
+  char* ws = static_cast<char*>(workspace);
+  prm.ws_parts = reinterpret_cast<int32_t*>(ws);
+  prm.ws_ml = reinterpret_cast<float*>(ws + pl.parts_bytes);
+  prm.ws_o = reinterpret_cast<float*>(ws + pl.parts_bytes + pl.ml_bytes);
+  prm.B = num_seqs;
+  prm.Hq = num_heads;
+  prm.Hkv = num_kv_heads;
+  prm.G = num_heads / num_kv_heads;
+  prm.ng = num_groups;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.bs = block_size;
+  prm.num_blocks = num_blocks;
+  prm.ps_blocks = pl.ps_blocks;
+  prm.pt_tokens = pl.pt_tokens;
+  prm.max_parts = pl.max_parts;
+  prm.tile_bytes = (uint32_t)(block_size * head_dim * 2);
+  prm.qscale = scale * kLog2eS;
+
+  // Stages of four tiles: as many as fit beside the tables for two CTAs per
+  // SM (2..6), or, when a stage is so large that two do not fit, one CTA
+  // per SM with up to 3.
+  // shared memory: stages (K and V tiles), their two mbarriers each, the
+  // abort flag (16 bytes), then the tables: wsum[8], Ls[B], preT[B+1],
+  // gsm[ngMax+1], preG[ngMax+1], shc[ngMax], Sg[ngMax]
+  const size_t stage = 2 * (size_t)kTiles * prm.tile_bytes;
+  const size_t ngMax = (size_t)(num_groups > num_seqs ? num_groups : num_seqs);
+  const size_t tables = 16 + 4 * (8 + 2 * (size_t)num_seqs + 1 + 4 * ngMax + 2);
+  const size_t per_cta = (227 * 1024) / 2 - 1024;
+  int ns = (int)((per_cta - tables - kAlign) / (stage + 16));
+  if (ns >= 2) {
+    if (ns > 6) ns = 6;
+  } else {
+    ns = (int)((227 * 1024 - tables - kAlign) / (stage + 16));
+    if (ns > 3) ns = 3;
+    if (ns < 1) return PA_ERR_SHAPE;
+  }
+  prm.nstage = ns;
+  const size_t smem = (size_t)ns * (stage + 2 * sizeof(uint64_t)) + tables + kAlign;
+
+  const void* kern = head_dim == 64 ? reinterpret_cast<const void*>(&shared_decode_kernel<64>)
+                                    : reinterpret_cast<const void*>(&shared_decode_kernel<128>);
+  const void* merge = head_dim == 64 ? reinterpret_cast<const void*>(&shared_merge_kernel<64>)
+                                     : reinterpret_cast<const void*>(&shared_merge_kernel<128>);
+  const int occ = shared_occupancy(kern, smem, dev);
+  if (occ <= 0) return PA_ERR_CUDA;
+  const unsigned grid = (unsigned)(occ * device_sm_count());
+  void* args[] = {&mapK, &mapV, &prm};
+  if (!ck(cudaLaunchKernel(kern, dim3(grid), dim3(kST), args, smem, (cudaStream_t)stream),
+          "cudaLaunchKernel(shared_decode_kernel)"))
+    return PA_ERR_CUDA;
+  const long long warps = (long long)num_seqs * num_heads;
+  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  void* margs[] = {&prm};
+  if (!ck(cudaLaunchKernel(merge, dim3(blocks), dim3(256), margs, 0, (cudaStream_t)stream),
+          "cudaLaunchKernel(shared_merge_kernel)"))
+    return PA_ERR_CUDA;
+  return PA_OK;
+}

@@ -43,6 +43,13 @@ def test_workspace_and_partition_arithmetic(pa):
     assert pa.partition_size(64, 32, 8, 128, 128, 16, 0) == 2048
     assert pa.partition_size(64, 32, 32, 128, 128, 16, 64, fp8=True) == 64
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 0, fp8=True) == 12
+    # shared-prefix decode: per (sequence, head) slots for ceil(max_ctx / 256) + 1
+    # partitions, a partition count per sequence, never less than pa_decode's
+    rows = 512 * 32 * (1280 // 256 + 1)
+    assert pa.shared_workspace_bytes(512, 32, 8, 128, 80, 16, 0, 64) == 2048 + rows * 8 + rows * 128 * 4
+    assert pa.shared_workspace_bytes(64, 32, 32, 128, 128, 16, 0, 8) >= pa.workspace_bytes(64, 32, 32, 128, 128, 16)
+    # shapes the shared path does not take fall back to pa_decode's workspace
+    assert pa.shared_workspace_bytes(4, 64, 4, 128, 80, 16, 0, 1) == pa.workspace_bytes(4, 64, 4, 128, 80, 16, 0)
 
 
 def test_host_side_rejections_launch_nothing(pa):
@@ -87,6 +94,16 @@ def test_host_side_rejections_launch_nothing(pa):
     # copies accept e4m3 pools and the [NB, bs, 1, 1] fp32 scale rows, not blocks of a partial chunk
     assert L.pa_copy_blocks(fake, fake, fake, 0, 10, 16, 1, 1, 0, null) == 0
     assert L.pa_copy_blocks(fake, fake, fake, 0, 10, 4, 1, 1, 2, null) == -2      # 4 bytes per block
+    # shared-prefix decode: a descriptor is required when groups are named; the
+    # workspace is checked before anything is launched; partitions are whole blocks
+    assert L.pa_decode_shared(fake, fake, fake, fake, fake, 80, fake, 16, null, fake, 2, 32, 8, 128, 16, 10, 1.0,
+                              0, null, 0, 1, null) == -1
+    assert L.pa_decode_shared(fake, fake, fake, fake, fake, 80, fake, 16, fake, fake, 2, 32, 8, 128, 16, 10, 1.0,
+                              0, null, 0, 1, null) == -5
+    assert L.pa_decode_shared(fake, fake, fake, fake, fake, 80, fake, 16, fake, fake, 2, 32, 8, 128, 16, 10, 1.0,
+                              24, null, 0, 1, null) == -2
+    assert L.pa_decode_shared(fake, fake, fake, fake, fake, 80, fake, 16, fake, fake, -1, 32, 8, 128, 16, 10, 1.0,
+                              0, null, 0, 1, null) == -2
     # empty inputs are a no-op success
     assert L.pa_copy_blocks(null, null, null, 0, 10, 16, 2, 64, 1, null) == 0
     assert L.pa_swap_blocks(null, null, 4, null, null, 10, null, 0, 16, 2, 64, 1, null) == 0
