@@ -128,10 +128,12 @@ __device__ __forceinline__ int shared_items_per_part(const SParams& p, int R) {
   return ceil_div(R, 32) * ceil_div(p.Hkv, 2);
 }
 
-// Block-wide exclusive scan of arr[0..n) in place; arr[n] = total.
+// Block-wide exclusive scan of arr[0..n) in place (NTH threads, all of the
+// block); arr[n] = total.
+template <int NTH>
 __device__ void block_scan(int* arr, int n, int* wsum) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = (n + kST - 1) / kST;
+  const int per = (n + NTH - 1) / NTH;
   const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
   int sum = 0;
   for (int i = i0; i < i1; ++i) sum += arr[i];
@@ -150,8 +152,69 @@ __device__ void block_scan(int* arr, int n, int* wsum) {
     arr[i] = run;
     run += c;
   }
-  if (threadIdx.x == kST - 1) arr[n] = run;
+  if (threadIdx.x == NTH - 1) arr[n] = run;
   __syncthreads();
+}
+
+// Items of one shared partition of a group with R rows per KV head, and of
+// one tail partition (KV heads grouped as the stages hold them).
+__device__ __forceinline__ int part_items(const SParams& p, int R, bool shared) {
+  return shared ? shared_items_per_part(p, R) : ceil_div(p.Hkv, 4);
+}
+
+// Every CTA builds the same tables (all NTH threads take part): the clamped
+// lengths, the group descriptor (checked: non-decreasing from 0 to B,
+// otherwise every sequence is its own group and PA_DEV_BAD_GROUP is set), the
+// shared blocks used per group, the partitions of every sequence (written to
+// the workspace by CTA 0 for the merge), item counts and their prefix sums.
+// Returns the number of items.
+template <int NTH>
+__device__ int build_tables(const SParams& p, Tables& t, int* wsum) {
+  const int Lmax = p.max_blocks * p.bs;
+  for (int b = threadIdx.x; b < p.B; b += NTH) {
+    int L = __ldg(&p.context_lens[b]);
+    if (L < 0 || L > Lmax) {
+      if (blockIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_LEN);
+      L = L < 0 ? 0 : Lmax;
+    }
+    t.Ls[b] = L;
+  }
+  bool ok = true;
+  for (int g = threadIdx.x; g < p.ng; g += NTH) {
+    const int a = __ldg(&p.group_start[g]), c = __ldg(&p.group_start[g + 1]);
+    if (a > c || a < 0 || c > p.B) ok = false;
+  }
+  if (threadIdx.x == 0 && (__ldg(&p.group_start[0]) != 0 || __ldg(&p.group_start[p.ng]) != p.B)) ok = false;
+  const bool valid = __syncthreads_and(ok) != 0;
+  if (!valid && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_GROUP);
+  t.ngE = valid ? p.ng : p.B;
+  for (int g = threadIdx.x; g <= t.ngE; g += NTH) t.gsm[g] = valid ? __ldg(&p.group_start[g]) : g;
+  __syncthreads();
+  const int ipt = part_items(p, p.G, false);
+  for (int g = threadIdx.x; g < t.ngE; g += NTH) {
+    const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
+    int S = 0;
+    if (valid && s1 - s0 >= 2) {
+      S = min(max(__ldg(&p.shared_blocks[g]), 0), p.max_blocks);
+      for (int b = s0; b < s1; ++b) S = min(S, t.Ls[b] / p.bs);
+    }
+    t.Sg[g] = S;
+    const int nspg = S > 0 ? ceil_div(S, p.ps_blocks) : 0;
+    t.shc[g] = nspg * part_items(p, (s1 - s0) * p.G, true);
+    int tsum = 0;
+    for (int b = s0; b < s1; ++b) {
+      int nsp, ntp;
+      seq_parts(p, S, t.Ls[b], nsp, ntp);
+      t.preT[b] = ntp * ipt;
+      tsum += ntp * ipt;
+      if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
+    }
+    t.preG[g] = t.shc[g] + tsum;
+  }
+  __syncthreads();
+  block_scan<NTH>(t.preT, p.B, wsum);
+  block_scan<NTH>(t.preG, t.ngE, wsum);
+  return t.preG[t.ngE];
 }
 
 // Item i -> its description (every role computes the same).
@@ -228,6 +291,161 @@ __device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i,
   }
 }
 
+// 2^x by the MUFU instruction (flush-to-zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The exponent reference of a column moves only when a score exceeds it by
+// more than 2^kTau (base-2 units), so most steps need neither the
+// cross-lane maximum nor a rescale of the accumulators; weights stay below
+// 2^kTau, far inside fp32 and bf16 range.  Any reference gives the same
+// normalised result (the online softmax is exact for any choice of m).
+constexpr float kTau = 8.f;
+
+// Two 16-token chunks per online-softmax step (1) or one (0; measured faster:
+// the pair's extra registers spill at the two-CTA-per-SM budget).
+#ifndef PA_SHARED_PAIR
+#define PA_SHARED_PAIR 0
+#endif
+
+// KB chunks of up to 16 tokens each (one online-softmax step over all of
+// them) for NT n-tiles of 8 query rows: S^T = K Q^T with the chunk's tokens as
+// the M rows, the column reference check, then O^T += V^T P.  Chunk k: K and
+// V tiles at kt[k], vt[k] (128-byte-swizzled 64-column spans of bs rows),
+// tokens tb[k] .. tb[k]+15 of the tile, the first valid[k] - tb[k] of them
+// real (FULL: all 16).  When fewer than four accumulation chains would run
+// (KB * NT < 4), the k-steps alternate between two accumulators so that
+// consecutive MMAs do not wait on each other.
+template <int D, int NT, int KB, bool FULL>
+__device__ __forceinline__ void step_chunks(const uint32_t (&kt)[KB], const uint32_t (&vt)[KB], const int (&tb)[KB],
+                                            const int (&valid)[KB], int bs, uint32_t half_bytes, float qscale,
+                                            const uint32_t (&qb)[NT][D / 16][2], float (&OT)[D / 16][NT][4],
+                                            float (&mh)[NT][2], float (&lh)[NT][2]) {
+  constexpr int KS = D / 16;
+  constexpr int MT = D / 16;
+  constexpr bool SPLIT = KB * NT < 4;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  float St[KB][NT][4];
+  float Su[KB][NT][4];            // odd k-steps when SPLIT
+#pragma unroll
+  for (int k = 0; k < KB; ++k)
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) St[k][n][e] = Su[k][n][e] = 0.f;
+  {
+    // K rows as the A fragment: lanes 0-7 tokens tb..+7, chunk 2kk; 8-15
+    // tokens tb+8..+15, chunk 2kk; 16-31 the same for chunk 2kk+1.  Tokens
+    // tb[k] + r share the swizzle phase of tb[0] + r (tb is a multiple of 16).
+    uint32_t krow[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      const int tt = min(tb[k] + (lane & 7) + (((lane >> 3) & 1) << 3), bs - 1);
+      krow[k] = kt[k] + tt * 128;
+    }
+    const int tsw = (min(tb[0] + (lane & 7) + (((lane >> 3) & 1) << 3), bs - 1)) & 7;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int c = 2 * kk + (lane >> 4);
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        uint32_t a[4];
+        ldsm_x4(krow[k] + (c >> 3) * half_bytes + (((c & 7) ^ tsw) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          if (SPLIT && (kk & 1)) mma_bf16_16816(Su[k][n], a, qb[n][kk][0], qb[n][kk][1]);
+          else mma_bf16_16816(St[k][n], a, qb[n][kk][0], qb[n][kk][1]);
+        }
+      }
+    }
+  }
+  uint32_t pb[KB][NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    float lmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      const bool ok0 = FULL || tb[k] + g < valid[k], ok1 = FULL || tb[k] + g + 8 < valid[k];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v = (SPLIT ? St[k][n][e] + Su[k][n][e] : St[k][n][e]) * qscale;
+        St[k][n][e] = FULL ? v : ((e < 2 ? ok0 : ok1) ? v : -INFINITY);
+      }
+      lmax[0] = fmaxf(lmax[0], fmaxf(St[k][n][0], St[k][n][2]));
+      lmax[1] = fmaxf(lmax[1], fmaxf(St[k][n][1], St[k][n][3]));
+    }
+    const bool need = lmax[0] > mh[n][0] + kTau || lmax[1] > mh[n][1] + kTau;
+    if (__any_sync(0xffffffffu, need)) {
+      float alpha[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float m_ = lmax[e];
+        m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 4));
+        m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 8));
+        m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, 16));
+        alpha[e] = 1.f;
+        if (m_ > mh[n][e] + kTau) {
+          alpha[e] = ex2f(mh[n][e] - m_);        // 0 when there was no reference yet
+          mh[n][e] = m_;
+          lh[n][e] *= alpha[e];
+        }
+      }
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          OT[m][n][0] *= alpha[0];
+          OT[m][n][1] *= alpha[1];
+          OT[m][n][2] *= alpha[0];
+          OT[m][n][3] *= alpha[1];
+        }
+      }
+    }
+    // a column with no reference yet has seen only masked tokens: its
+    // weights are 2^-inf = 0 against any finite reference
+    const float r0 = mh[n][0] == -INFINITY ? 0.f : mh[n][0];
+    const float r1 = mh[n][1] == -INFINITY ? 0.f : mh[n][1];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      float pw[4];
+      pw[0] = ex2f(St[k][n][0] - r0);
+      pw[1] = ex2f(St[k][n][1] - r1);
+      pw[2] = ex2f(St[k][n][2] - r0);
+      pw[3] = ex2f(St[k][n][3] - r1);
+      lh[n][0] += pw[0] + pw[2];
+      lh[n][1] += pw[1] + pw[3];
+      pb[k][n][0] = movmatrix_t(pack_bf16(pw[0], pw[1]));   // tokens 0-7 of the chunk
+      pb[k][n][1] = movmatrix_t(pack_bf16(pw[2], pw[3]));   // tokens 8-15
+    }
+  }
+  {
+    // V^T as the A fragment (ldmatrix.trans): lanes 0-7 tokens tb..+7 chunk
+    // 2m; 8-15 the same tokens, chunk 2m+1; 16-31 tokens tb+8..+15, chunks
+    // 2m, 2m+1
+    uint32_t vrow[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      const int tt = min(tb[k] + (lane & 7) + ((lane >> 4) << 3), bs - 1);
+      vrow[k] = vt[k] + tt * 128;
+    }
+    const int tsw = (min(tb[0] + (lane & 7) + ((lane >> 4) << 3), bs - 1)) & 7;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const int c = 2 * m + ((lane >> 3) & 1);
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        uint32_t a[4];
+        ldsm_x4_t(vrow[k] + (c >> 3) * half_bytes + (((c & 7) ^ tsw) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) mma_bf16_16816(OT[m][n], a, pb[k][n][0], pb[k][n][1]);
+      }
+    }
+  }
+}
+
 // One consumer warp's share of an item: NT n-tiles (8 query rows each) of
 // KV head kvh0 + hd over the tiles hd*bps .. hd*bps+bps-1 of every stage.
 template <int D, int NT>
@@ -267,6 +485,7 @@ __device__ __forceinline__ void run_rows(const SParams& p, const Tables& t, cons
 #pragma unroll
   for (int n = 0; n < NT; ++n) mh[n][0] = mh[n][1] = -INFINITY, lh[n][0] = lh[n][1] = 0.f;
   const uint32_t half_bytes = (uint32_t)p.bs * 128u;
+  const int cpt = (p.bs + 15) >> 4;     // 16-token chunks per full tile
 
   const int nstages = ceil_div(it.je - it.jb, it.bps);
   for (int s = 0; s < nstages; ++s) {
@@ -288,98 +507,52 @@ __device__ __forceinline__ void run_rows(const SParams& p, const Tables& t, cons
       }
     }
     if (live && active) {
-#pragma unroll 1
-      for (int kb = 0; kb < it.bps; ++kb) {
-        const int j = it.jb + s * it.bps + kb;
-        if (j >= it.je) break;
-        const int valid = min(p.bs, it.t1 - j * p.bs);
-        const int tile = st * kTiles + hd * it.bps + kb;
-        unsigned char* vt_ptr = tilesV + (size_t)tile * p.tile_bytes;
-        const uint32_t kt = smem_u32(tilesK + (size_t)tile * p.tile_bytes);
-        const uint32_t vt = smem_u32(vt_ptr);
-        if (valid < p.bs) {
-          // slots past the context may hold anything; P is 0 there, but
-          // 0 * NaN is NaN inside the product, so clear those V rows.  Only
-          // tail tiles can be partial, and each of those has one reader.
-          for (int idx = lane; idx < (p.bs - valid) * (D / 8); idx += 32) {
-            const int tk = valid + idx / (D / 8), c = idx % (D / 8);
-            *reinterpret_cast<uint4*>(vt_ptr + (c >> 3) * half_bytes + tk * 128 + (c & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
+      const int j0 = it.jb + s * it.bps;
+      const int ntile = min(it.bps, it.je - j0);
+      const int tile0 = st * kTiles + hd * it.bps;
+      // slots past the context may hold anything; P is 0 there, but 0 * NaN
+      // is NaN inside the product, so clear those V rows.  Only a tail
+      // item's last tile can be partial, and it has one reader.
+      const int vlast = min(p.bs, it.t1 - (j0 + ntile - 1) * p.bs);
+      if (vlast < p.bs) {
+        unsigned char* vt_ptr = tilesV + (size_t)(tile0 + ntile - 1) * p.tile_bytes;
+        for (int idx = lane; idx < (p.bs - vlast) * (D / 8); idx += 32) {
+          const int tk = vlast + idx / (D / 8), c = idx % (D / 8);
+          *reinterpret_cast<uint4*>(vt_ptr + (c >> 3) * half_bytes + tk * 128 + (c & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
-        for (int tb = 0; tb < valid; tb += 16) {
-          float St[NT][4];
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // the stage's chunks of 16 tokens, two per online-softmax step
+      const int nch = (ntile - 1) * cpt + ((vlast + 15) >> 4);
+      const uint32_t kbase = smem_u32(tilesK + (size_t)tile0 * p.tile_bytes);
+      const uint32_t vbase = smem_u32(tilesV + (size_t)tile0 * p.tile_bytes);
+      int ci = 0;
+      for (; PA_SHARED_PAIR && ci + 1 < nch; ci += 2) {
+        uint32_t kt[2], vt[2];
+        int tb[2], vd[2];
 #pragma unroll
-          for (int n = 0; n < NT; ++n) St[n][0] = St[n][1] = St[n][2] = St[n][3] = 0.f;
-          {
-            // K rows as the A fragment: lanes 0-7 tokens tb..+7, chunk 2kk;
-            // 8-15 tokens tb+8..+15, chunk 2kk; 16-31 the same for chunk 2kk+1
-            const int tt = min(tb + (lane & 7) + (((lane >> 3) & 1) << 3), p.bs - 1);
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-              const int c = 2 * kk + (lane >> 4);
-              uint32_t a[4];
-              ldsm_x4(kt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), a[0], a[1], a[2], a[3]);
-#pragma unroll
-              for (int n = 0; n < NT; ++n) mma_bf16_16816(St[n], a, qb[n][kk][0], qb[n][kk][1]);
-            }
-          }
-          const bool ok0 = tb + g < valid, ok1 = tb + g + 8 < valid;
-          uint32_t pb[NT][2];
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            St[n][0] = ok0 ? St[n][0] * p.qscale : -INFINITY;
-            St[n][1] = ok0 ? St[n][1] * p.qscale : -INFINITY;
-            St[n][2] = ok1 ? St[n][2] * p.qscale : -INFINITY;
-            St[n][3] = ok1 ? St[n][3] * p.qscale : -INFINITY;
-            float alpha[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float mx = fmaxf(St[n][e], St[n][2 + e]);
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-              const float mn = fmaxf(mh[n][e], mx);
-              alpha[e] = mn == -INFINITY ? 1.f : exp2f(mh[n][e] - mn);
-              mh[n][e] = mn;
-              lh[n][e] *= alpha[e];
-            }
-            if (alpha[0] != 1.f || alpha[1] != 1.f) {
-#pragma unroll
-              for (int m = 0; m < MT; ++m) {
-                OT[m][n][0] *= alpha[0];
-                OT[m][n][1] *= alpha[1];
-                OT[m][n][2] *= alpha[0];
-                OT[m][n][3] *= alpha[1];
-              }
-            }
-            float pw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              pw[e] = St[n][e] == -INFINITY ? 0.f : exp2f(St[n][e] - mh[n][e & 1]);
-              lh[n][e & 1] += pw[e];
-            }
-            pb[n][0] = movmatrix_t(pack_bf16(pw[0], pw[1]));   // tokens 0-7
-            pb[n][1] = movmatrix_t(pack_bf16(pw[2], pw[3]));   // tokens 8-15
-          }
-          {
-            // V^T as the A fragment (ldmatrix.trans): lanes 0-7 tokens tb..+7
-            // chunk 2m; 8-15 the same tokens, chunk 2m+1; 16-31 tokens
-            // tb+8..+15, chunks 2m, 2m+1
-            const int tt = min(tb + (lane & 7) + ((lane >> 4) << 3), p.bs - 1);
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const int c = 2 * m + ((lane >> 3) & 1);
-              uint32_t a[4];
-              ldsm_x4_t(vt + (c >> 3) * half_bytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4), a[0], a[1], a[2],
-                        a[3]);
-#pragma unroll
-              for (int n = 0; n < NT; ++n) mma_bf16_16816(OT[m][n], a, pb[n][0], pb[n][1]);
-            }
-          }
+        for (int k = 0; k < 2; ++k) {
+          const int kb = (ci + k) / cpt;
+          tb[k] = ((ci + k) - kb * cpt) * 16;
+          vd[k] = kb == ntile - 1 ? vlast : p.bs;
+          kt[k] = kbase + (uint32_t)kb * p.tile_bytes;
+          vt[k] = vbase + (uint32_t)kb * p.tile_bytes;
         }
+        if (tb[0] + 16 <= vd[0] && tb[1] + 16 <= vd[1])
+          step_chunks<D, NT, 2, true>(kt, vt, tb, vd, p.bs, half_bytes, p.qscale, qb, OT, mh, lh);
+        else
+          step_chunks<D, NT, 2, false>(kt, vt, tb, vd, p.bs, half_bytes, p.qscale, qb, OT, mh, lh);
+      }
+      for (; ci < nch; ++ci) {
+        const int kb = ci / cpt;
+        uint32_t kt[1] = {kbase + (uint32_t)kb * p.tile_bytes}, vt[1] = {vbase + (uint32_t)kb * p.tile_bytes};
+        int tb[1] = {(ci - kb * cpt) * 16}, vd[1] = {kb == ntile - 1 ? vlast : p.bs};
+        if (tb[0] + 16 <= vd[0])
+          step_chunks<D, NT, 1, true>(kt, vt, tb, vd, p.bs, half_bytes, p.qscale, qb, OT, mh, lh);
+        else
+          step_chunks<D, NT, 1, false>(kt, vt, tb, vd, p.bs, half_bytes, p.qscale, qb, OT, mh, lh);
       }
     }
     __syncwarp();
@@ -464,53 +637,7 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
     fence_mbar_init();
   }
 
-  // ---- tables: clamped lengths, the group descriptor (checked), shared
-  // blocks per group, item counts, prefix sums
-  const int Lmax = p.max_blocks * p.bs;
-  for (int b = threadIdx.x; b < p.B; b += kST) {
-    int L = __ldg(&p.context_lens[b]);
-    if (L < 0 || L > Lmax) {
-      if (blockIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_LEN);
-      L = L < 0 ? 0 : Lmax;
-    }
-    t.Ls[b] = L;
-  }
-  bool ok = true;
-  for (int g = threadIdx.x; g < p.ng; g += kST) {
-    const int a = __ldg(&p.group_start[g]), c = __ldg(&p.group_start[g + 1]);
-    if (a > c || a < 0 || c > p.B) ok = false;
-  }
-  if (threadIdx.x == 0 && (__ldg(&p.group_start[0]) != 0 || __ldg(&p.group_start[p.ng]) != p.B)) ok = false;
-  const bool valid = __syncthreads_and(ok) != 0;
-  if (!valid && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_GROUP);
-  t.ngE = valid ? p.ng : p.B;
-  for (int g = threadIdx.x; g <= t.ngE; g += kST) t.gsm[g] = valid ? __ldg(&p.group_start[g]) : g;
-  __syncthreads();
-  const int ipt = ceil_div(p.Hkv, 4);        // tail items per tail partition
-  for (int g = threadIdx.x; g < t.ngE; g += kST) {
-    const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
-    int S = 0;
-    if (valid && s1 - s0 >= 2) {
-      S = min(max(__ldg(&p.shared_blocks[g]), 0), p.max_blocks);
-      for (int b = s0; b < s1; ++b) S = min(S, t.Ls[b] / p.bs);
-    }
-    t.Sg[g] = S;
-    const int nspg = S > 0 ? ceil_div(S, p.ps_blocks) : 0;
-    t.shc[g] = nspg * shared_items_per_part(p, (s1 - s0) * p.G);
-    int tsum = 0;
-    for (int b = s0; b < s1; ++b) {
-      int nsp, ntp;
-      seq_parts(p, S, t.Ls[b], nsp, ntp);
-      t.preT[b] = ntp * ipt;
-      tsum += ntp * ipt;
-      if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
-    }
-    t.preG[g] = t.shc[g] + tsum;
-  }
-  __syncthreads();
-  block_scan(t.preT, p.B, wsum);
-  block_scan(t.preG, t.ngE, wsum);
-  const int n_items = t.preG[t.ngE];
+  const int n_items = build_tables<kST>(p, t, wsum);
 
   if (warp == kSW) {
     // ------------------------------------------------------------ producer
@@ -616,10 +743,13 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   }
 }
 
-// One warp per (sequence, query head) whose sequence has several partitions.
+// One warp per (sequence, query head) whose sequence has several partitions:
+// out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i with M = max_i m_i.
+// Lane i < 32 computes part i's weight; each part's row of o is read as one
+// 16-byte (head_dim 128) or 8-byte vector per lane.
 template <int D>
 __global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
-  constexpr int PER = D / 32;
+  constexpr int VPL = D / 32;      // dims per lane
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= (long long)p.B * p.Hq) return;
@@ -632,25 +762,47 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float den = 0.f;
-  for (int i = lane; i < nparts; i += 32) {
-    const float mi = p.ws_ml[(base + i) * 2];
-    if (mi != -INFINITY) den += exp2f(mi - M) * p.ws_ml[(base + i) * 2 + 1];
+  float acc[VPL];
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
+  for (int i0 = 0; i0 < nparts; i0 += 32) {
+    const int i = i0 + lane;
+    float w = 0.f;
+    if (i < nparts) {
+      const float mi = p.ws_ml[(base + i) * 2];
+      w = mi == -INFINITY ? 0.f : exp2f(mi - M);
+      den = fmaf(w, p.ws_ml[(base + i) * 2 + 1], den);
+    }
+    const int cnt = min(32, nparts - i0);
+    const float* o = p.ws_o + (base + i0) * D + lane * VPL;
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      if constexpr (VPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(o + (size_t)k * D);
+        acc[0] = fmaf(wk, v.x, acc[0]);
+        acc[1] = fmaf(wk, v.y, acc[1]);
+        acc[2] = fmaf(wk, v.z, acc[2]);
+        acc[3] = fmaf(wk, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(o + (size_t)k * D);
+        acc[0] = fmaf(wk, v.x, acc[0]);
+        acc[1] = fmaf(wk, v.y, acc[1]);
+      }
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  float acc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  for (int i = 0; i < nparts; ++i) {
-    const float mi = p.ws_ml[(base + i) * 2];
-    const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
-    const float* oi = p.ws_o + (base + i) * D;
-#pragma unroll
-    for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oi[lane + 32 * k], acc[k]);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)gw * D + lane * VPL;
+  if constexpr (VPL == 4) {
+    uint2 v;
+    v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(out) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(out) = pack_bf16(acc[0] * inv, acc[1] * inv);
   }
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)gw * D;
-#pragma unroll
-  for (int k = 0; k < PER; ++k) out[lane + 32 * k] = __float2bfloat16_rn(den > 0.f ? acc[k] / den : 0.f);
 }
 
 // ------------------------------------------------------------------ host side
@@ -822,9 +974,9 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   prm.tile_bytes = (uint32_t)(block_size * head_dim * 2);
   prm.qscale = scale * kLog2eS;
 
-  // Stages of four tiles: as many as fit beside the tables for two CTAs per
-  // SM (2..6), or, when a stage is so large that two do not fit, one CTA
-  // per SM with up to 3.
+  // Stages of four tiles: as many as fit beside
+  // the tables for two CTAs per SM (2..6), or, when a stage is so large that
+  // two do not fit, one CTA per SM with up to 3.
   // shared memory: stages (K and V tiles), their two mbarriers each, the
   // abort flag (16 bytes), then the tables: wsum[8], Ls[B], preT[B+1],
   // gsm[ngMax+1], preG[ngMax+1], shc[ngMax], Sg[ngMax]

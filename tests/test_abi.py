@@ -49,7 +49,8 @@ def test_workspace_and_partition_arithmetic(pa):
     assert pa.shared_workspace_bytes(512, 32, 8, 128, 80, 16, 0, 64) == 2048 + rows * 8 + rows * 128 * 4
     assert pa.shared_workspace_bytes(64, 32, 32, 128, 128, 16, 0, 8) >= pa.workspace_bytes(64, 32, 32, 128, 128, 16)
     # shapes the shared path does not take fall back to pa_decode's workspace
-    assert pa.shared_workspace_bytes(4, 64, 4, 128, 80, 16, 0, 1) == pa.workspace_bytes(4, 64, 4, 128, 80, 16, 0)
+    assert pa.shared_workspace_bytes(4, 256, 4, 128, 80, 16, 0, 1) == pa.workspace_bytes(4, 256, 4, 128, 80, 16, 0)
+    assert pa.shared_workspace_bytes(4, 64, 4, 64, 80, 16, 0, 1) == pa.workspace_bytes(4, 64, 4, 64, 80, 16, 0)
 
 
 def test_host_side_rejections_launch_nothing(pa):

@@ -56,9 +56,9 @@ def test_shared_matches_oracle_c5_small(pa, partition):
 
 
 # (Hq, Hkv, head_dim, block_size, samples, prefix tokens, max tail):
-# one warp per head with 8 rows (MHA, 8 samples), 16 rows (G = 2), two warps
-# per head (32 rows), row chunks (64 rows), head_dim 64 with block_size 8,
-# KV heads not a multiple of 4, odd sample counts, block_size 32
+# 8 rows per KV head (MHA, 8 samples), 16 (G = 2), 32, row chunks (64
+# rows), head_dim 64 with block_size 8, KV heads not a multiple of 4, odd
+# sample counts, prompts that end inside a block, block sizes 8 and 32
 SHAPES = [
     (32, 8, 128, 16, 8, 128, 40),
     (8, 8, 128, 16, 8, 96, 30),
@@ -68,6 +68,8 @@ SHAPES = [
     (24, 6, 128, 32, 3, 96, 70),
     (12, 6, 128, 16, 5, 48, 33),
     (4, 4, 128, 16, 2, 32, 17),
+    (32, 8, 128, 8, 8, 200, 60),
+    (32, 8, 128, 32, 8, 160, 100),
 ]
 
 
@@ -225,8 +227,9 @@ def test_shared_graph_replay_is_bit_identical(pa):
 
 
 def test_unsupported_shapes_run_plain_decode(pa):
-    # fp32 pools and groups of 16 query heads take pa_decode's path unchanged
-    for name, over in (("c1", {}), ("c4", {"Hq": 64, "Hkv": 4})):
+    # fp32 pools and groups of more than 8 query heads take pa_decode's path
+    # unchanged
+    for name, over in (("c1", {}), ("c4", {"Hq": 64, "Hkv": 4, "D": 64}), ("c4", {"Hq": 128, "Hkv": 2})):
         c = W.decode_case(name, small=True, device="cuda", **over)
         pa.reshape_and_cache(c.key, c.value, c.slot_mapping, c.k_cache, c.v_cache)
         B = c.q.shape[0]
