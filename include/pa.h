@@ -312,8 +312,9 @@ int pa_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks,
  *    with PA_ERR_WORKSPACE (nothing launched; pa_last_host_error() says how
  *    much was needed).
  *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it, and so does the first call after
+ *    the device's context has changed (e.g. after cudaDeviceReset()); make
+ *    such a call before any stream capture.
  *  - Every call on a device shares the one array and it keeps the previous
  *    call's contents: calls whose GPU work overlaps (e.g. on two streams)
  *    race on it and must be ordered by the caller.  Nothing in it needs to
@@ -350,7 +351,9 @@ int pa_decode_fp8_partition_size(int num_seqs, int num_heads, int num_kv_heads, 
  * block pairs[2i] (all block_size slots, all heads).
  *
  *   pairs   [num_pairs, 2] int64 (src, dst), device memory.  dsts must be
- *           distinct and no dst may be the src of another pair.
+ *           distinct and no dst may be the src of another pair; if they are
+ *           not, the contents of the blocks involved are undefined (nothing
+ *           is flagged).  A pair whose src equals its dst changes nothing.
  *
  * A pair with an id outside [0, num_blocks) is skipped and sets
  * PA_DEV_BAD_BLOCK.  num_pairs == 0 launches nothing.

@@ -135,6 +135,7 @@ copy_blocks_kernel(unsigned char* __restrict__ k_cache, unsigned char* __restric
     if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(&g_status_cache, PA_DEV_BAD_BLOCK);
     return;
   }
+  if (src == dst) return;     // a block copied onto itself is unchanged (and would alias the restrict operands)
   unsigned char* base = blockIdx.y == 0 ? k_cache : v_cache;
   const long long off = (long long)blockIdx.z * span_bytes;
   const long long n = block_bytes - off < span_bytes ? block_bytes - off : span_bytes;

@@ -383,18 +383,43 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {};
+void* g_scratch_ctx[64] = {};
+
+// The driver's current context (cuCtxGetCurrent through the runtime's
+// driver entry point); null if it cannot be read.
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (Fn) nullptr;
+    return reinterpret_cast<Fn>(p);
+  }();
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address has to come
-// from cudaGetSymbolAddress, once per device, with that device current.
+// from cudaGetSymbolAddress, with that device current.  It is looked up on
+// the first call on a device and again whenever the device's context has
+// changed since (a cudaDeviceReset() reloads the module at a new address).
 void* scratch_address(int dev) {
-  if (dev < 0 || dev >= 64) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    note_host_error("pa_decode_noalloc: device ordinals of 64 and above are not supported");
+    return nullptr;
+  }
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || ctx != g_scratch_ctx[dev]) {
     void* ptr = nullptr;
     if (!ck(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress(no-alloc scratch)"))
       return nullptr;
     g_scratch_ptr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   return g_scratch_ptr[dev];
 }

@@ -82,6 +82,16 @@ def test_copy_blocks_fp32_and_bad_pair(pa):
     assert np.array_equal(bits(k), exp_k) and np.array_equal(bits(v), exp_v)
 
 
+def test_copy_blocks_onto_itself_changes_nothing(pa):
+    g = torch.Generator(device="cuda").manual_seed(8)
+    k = torch.randn(6, 16, 2, 64, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(6, 16, 2, 64, device="cuda", generator=g).to(torch.bfloat16)
+    before_k, before_v = bits(k), bits(v)
+    pa.copy_blocks(k, v, torch.tensor([[4, 4], [2, 2]], dtype=torch.int64, device="cuda"))
+    assert pa.last_error() == 0
+    assert np.array_equal(bits(k), before_k) and np.array_equal(bits(v), before_v)
+
+
 @pytest.mark.parametrize("dtype,bs,H,D", [("bf16", 16, 8, 128), ("f32", 16, 2, 64), ("bf16", 32, 8, 128),
                                          ("bf16", 4, 1, 32)])
 def test_swap_out_to_pinned_host_and_back(pa, dtype, bs, H, D):
@@ -329,11 +339,24 @@ def test_full_size_sampled(pa, name):
     _full_check(pa, name)
 
 
+@pytest.mark.parametrize("partition", [0, 512])
 @pytest.mark.parametrize("name", ["c4", "c4b32"])
-def test_full_size_gqa_split_sampled(pa, name):
-    (_, c, out) = _full_check(pa, name, n_sample=3)
+def test_full_size_gqa_split_sampled(pa, name, partition):
+    # automatic (2048-token) partitions and the configuration's 512-token ones
+    (_, c, out) = _full_check(pa, name, n_sample=3, partition=partition)
     del c, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("lens", [[511, 512, 513, 1024, 1537], [2047, 2048, 2049, 1, 4095]])
+@pytest.mark.parametrize("partition", [512, 2048])
+def test_gqa_ragged_partition_boundaries(pa, lens, partition):
+    # grouped-query path (tokens in M) across 512- and 2048-token partition edges
+    c = _cuda_case("c4", lens=lens)
+    ref = oracle_decode(c)
+    out = gpu_decode(c, partition_size=partition)
+    assert pa.last_error() == 0
+    assert_close(f64(out), ref, "bf16")
 
 
 def test_full_c2_split_equals_unsplit(pa):

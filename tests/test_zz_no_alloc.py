@@ -3,10 +3,10 @@ when they call in (a plug-in whose host engine owns all device allocations,
 or a latency-critical path that cannot risk an allocation call that may
 synchronise the device).  It uses a scratch array built into the library
 instead of a workspace.  These tests call it through the C ABI and check it
-against pa_decode with a caller-provided workspace, on two calls in a row
-(the array keeps the previous call's contents, which must not leak into the
-next result).  This file sorts last so that a run stopping at the first
-failure has already run every other test."""
+bit for bit against pa_decode with a caller-provided workspace, on two
+different calls in a row (the array keeps the previous call's contents,
+which must not leak into the next result).  This file sorts last so that a
+run stopping at the first failure has already run every other test."""
 
 import ctypes
 
@@ -39,19 +39,28 @@ def _noalloc(pa, out, c, partition):
                                     ctypes.c_float(c.scale), partition, pa.PA_BF16, ctypes.c_void_p(s.cuda_stream))
 
 
-@pytest.mark.parametrize("name,partition", [("c2", 0), ("c4", 0), ("c3", 64)])
-def test_noalloc_matches_workspace_decode_on_two_calls(pa, name, partition):
-    c = W.decode_case(name, small=True, device="cuda")
-    pa.reshape_and_cache(c.key, c.value, c.slot_mapping, c.k_cache, c.v_cache)
+def _reference(pa, c, partition):
     ref = torch.empty_like(c.q)
-    pa.decode(ref, c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale,
-              partition_size=partition)
+    pa.decode(ref, c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale, partition_size=partition)
     torch.cuda.synchronize()
-    for _ in range(2):
+    return ref
+
+
+# Two calls in a row on different cases: the second has fewer partitions per
+# sequence than the first left in the array, so stale partials from the first
+# call would change its result if they leaked into the merge.
+@pytest.mark.parametrize("first,second", [(("c4", 0), ("c3", 64)), (("c2", 16), ("c2", 0)), (("c3", 64), ("c4", 512))])
+def test_noalloc_matches_workspace_decode_on_two_calls(pa, first, second):
+    for name, partition in (first, second):
+        c = W.decode_case(name, small=True, device="cuda")
+        pa.reshape_and_cache(c.key, c.value, c.slot_mapping, c.k_cache, c.v_cache)
+        ref = _reference(pa, c, partition)
         out = torch.full_like(c.q, float("nan"))
         assert _noalloc(pa, out, c, partition) == 0
         torch.cuda.synchronize()
         assert pa.last_error() == 0
+        # the same kernels over the same partitions: bit-identical
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (name, partition)
         assert_close(f64(out), f64(ref), "bf16")
 
 
