@@ -112,22 +112,24 @@ def _csrc(*names):
     return [os.path.join(ROOT, "paged_kv_cache_307_gb300", "csrc", f) for f in names]
 
 
-DECODE_SOURCES = _csrc("pa_decode_kernel.cuh", "pa_decode.cu")
-FP8_SOURCES = _csrc("pa_decode_kernel.cuh", "pa_decode.cu", "pa_decode_fp8.cu")
-SHARED_SOURCES = _csrc("pa_decode_shared.cu", "pa_mma.cuh")
+DECODE_SOURCES = _csrc("pa_decode_kernel.cuh", "pa_decode.cu", "pa_mma.cuh", "pa_common.cuh")
+FP8_SOURCES = _csrc("pa_decode_kernel.cuh", "pa_decode.cu", "pa_decode_fp8.cu", "pa_mma.cuh", "pa_common.cuh")
+SHARED_SOURCES = _csrc("pa_decode_shared.cu", "pa_mma.cuh", "pa_common.cuh")
 
 
-def traffic_record(workload, sources=DECODE_SOURCES):
-    """ncu DRAM bytes per launch of the decode kernel, from a committed
-    profile summary (scaled to the bench's launch as the summary states);
-    None if it is missing or the kernel changed since."""
+def traffic_record(workload, batch, sources=DECODE_SOURCES):
+    """ncu DRAM bytes per launch of the decode kernel for the full-size bench
+    workload, from a committed profile summary (captured at a smaller batch and
+    scaled by algorithmic bytes where the summary says so); None if it is
+    missing, is for another batch, or the kernel sources changed since."""
     p = os.path.join(ROOT, "profiles", "decode_%s_traffic.json" % workload)
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    h = kernel_hash(sources)
-    return d.get("traffic_bytes_per_launch") if d.get("kernel_sha256") == h else None
+    if d.get("batch") != batch or d.get("kernel_sha256") != kernel_hash(sources):
+        return None
+    return d.get("traffic_bytes_per_launch")
 
 
 class ClockSampler:
@@ -977,7 +979,7 @@ def run_ours(args, rank, world, local_rank):
         return
     peak, peak_src = peaks()
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    traffic = traffic_record(args.workload, SHARED_SOURCES if shared else FP8_SOURCES if fp8 else DECODE_SOURCES)
+    traffic = traffic_record(args.workload, Bsz, SHARED_SOURCES if shared else FP8_SOURCES if fp8 else DECODE_SOURCES)
     kname = ("pa_decode_shared (shared_decode_kernel + shared_merge_kernel)" if shared else
              "pa_decode_fp8 (decode_kernel + merge_kernel)" if fp8 else "pa_decode (decode_kernel + merge_kernel)")
     line = {
