@@ -1317,12 +1317,15 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   }
 }
 
-// One warp per (sequence, query head) with more than one partition.
+// One warp per (sequence, query head) with more than one partition:
+// out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i with M = max_i m_i.
+// Lane i < 32 computes partition i's weight (broadcast by shuffle); each
+// partition's row of o is read as one vector of D/32 floats per lane.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 merge_kernel(const DecodeParams p) {
   using E = Elem<T>;
-  constexpr int PER = D / 32;
+  constexpr int VPL = D / 32;                 // dims per lane: 4, 2 or 1
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= (long long)p.B * p.Hq) return;
@@ -1338,25 +1341,43 @@ merge_kernel(const DecodeParams p) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float den = 0.f;
-  for (int i = lane; i < nparts; i += 32) {
-    const float mi = p.ws_ml[(base + i) * 2];
-    if (mi != -INFINITY) den += exp2f(mi - M) * p.ws_ml[(base + i) * 2 + 1];
+  float acc[VPL];
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
+  for (int i0 = 0; i0 < nparts; i0 += 32) {
+    const int i = i0 + lane;
+    float w = 0.f;
+    if (i < nparts) {
+      const float mi = p.ws_ml[(base + i) * 2];
+      w = mi == -INFINITY ? 0.f : exp2f(mi - M);
+      den = fmaf(w, p.ws_ml[(base + i) * 2 + 1], den);
+    }
+    const int cnt = min(32, nparts - i0);
+    const float* o = p.ws_o + (base + i0) * D + lane * VPL;
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      if constexpr (VPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(o + (size_t)k * D);
+        acc[0] = fmaf(wk, v.x, acc[0]);
+        acc[1] = fmaf(wk, v.y, acc[1]);
+        acc[2] = fmaf(wk, v.z, acc[2]);
+        acc[3] = fmaf(wk, v.w, acc[3]);
+      } else if constexpr (VPL == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(o + (size_t)k * D);
+        acc[0] = fmaf(wk, v.x, acc[0]);
+        acc[1] = fmaf(wk, v.y, acc[1]);
+      } else {
+        acc[0] = fmaf(wk, o[(size_t)k * D], acc[0]);
+      }
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  float acc[PER];
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  T* out = static_cast<T*>(p.out) + (size_t)gw * D + lane * VPL;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  for (int i = 0; i < nparts; ++i) {
-    const float mi = p.ws_ml[(base + i) * 2];
-    const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
-    const float* oi = p.ws_o + (base + i) * D;
-#pragma unroll
-    for (int k = 0; k < PER; ++k) acc[k] = fmaf(w, oi[lane + 32 * k], acc[k]);
-  }
-  T* out = static_cast<T*>(p.out) + (size_t)gw * D;
-#pragma unroll
-  for (int k = 0; k < PER; ++k) E::store1(out + lane + 32 * k, den > 0.f ? acc[k] / den : 0.f);
+  for (int k = 0; k < VPL; ++k) E::store1(out + k, acc[k] * inv);
 }
 
 }  // namespace
