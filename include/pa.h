@@ -120,9 +120,13 @@ int pa_reshape_and_cache(const void* key, const void* value,
  *   context_lens   [num_seqs] int32
  *   scale          the pages use 1/sqrt(head_dim)
  *   partition_size split-K partition in tokens: 0 = automatic (256 tokens
- *                  when num_heads == num_kv_heads, 2048 for grouped-query
- *                  attention), < 0 = never split, > 0 = a multiple of
- *                  block_size.  A sequence longer
+ *                  when num_heads == num_kv_heads; 2048 for grouped-query
+ *                  attention, unless num_seqs * ceil(num_kv_heads / 4) <
+ *                  912, the unsplit work items being fewer than three per
+ *                  CTA of the grid: then the largest power of two from
+ *                  256 to 2048 not above max_blocks_per_seq * block_size *
+ *                  num_seqs * ceil(num_kv_heads / 4) / 2432, or 256), < 0 = never
+ *                  split, > 0 = a multiple of block_size.  A sequence longer
  *                  than one partition is processed as independent partitions
  *                  whose (max, sum, unnormalised output) states are merged by
  *                  log-sum-exp in a second kernel.
@@ -247,8 +251,8 @@ int pa_reshape_and_cache_fp8(const void* key, const void* value,
  *   k_cache, v_cache  e4m3 pools; k_scale, v_scale as written by
  *                     pa_reshape_and_cache_fp8 (16-byte aligned)
  *   partition_size    as for pa_decode, but the automatic choice is 512
- *                     tokens when num_heads == num_kv_heads (2048 for
- *                     grouped-query attention); pa_decode_fp8_partition_size
+ *                     tokens when num_heads == num_kv_heads (grouped-query
+ *                     attention as for pa_decode); pa_decode_fp8_partition_size
  *                     returns the size used
  *   workspace         pa_decode_workspace_bytes() with the same sizes is
  *                     enough (the automatic partition here is never shorter
@@ -406,8 +410,9 @@ int pa_prefill_paged(void* out, const void* query, int num_queries,
  *   out, query     [total_queries, num_heads, head_dim], rows in sequence
  *                  order: sequence b's rows start at query_start[b]
  *   query_start    [num_seqs + 1] int32, device, non-decreasing, starting
- *                  at 0 and ending at total_queries (a decreasing pair sets
- *                  PA_DEV_BAD_LEN and that sequence writes nothing)
+ *                  at 0 and ending at total_queries (a decreasing pair, or
+ *                  a start outside 0..total_queries, sets PA_DEV_BAD_LEN
+ *                  and that sequence writes nothing)
  *   other arguments as for pa_prefill_paged; num_seqs <= 2048
  *
  * The same tcgen05 kernel as pa_prefill_paged: each (query tile, KV head)

@@ -148,15 +148,37 @@ int fp8_heads_per_item(int num_kv_heads) {
   return hg;
 }
 
-// Automatic split: 2048 tokens for GQA, whose items already cover several
-// query heads per K/V read; for MHA 256 tokens over 16-bit pools (finer items
-// balance the persistent grid better than 512: c2 +0.5 %, c3 +1.3 %) and 512
-// over e4m3 pools, where an item's fixed costs (table read, lane and warp
-// merges, the partial's write) weigh on half the bytes (c2 over e4m3: +7 %).
-int resolve_partition(int max_blocks, int bs, int partition_size, int G, bool fp8) {
+// Automatic split.  MHA: 256 tokens over 16-bit pools (finer items balance
+// the persistent grid better than 512: c2 +0.5 %, c3 +1.3 %) and 512 over
+// e4m3 pools, where an item's fixed costs (table read, lane and warp merges,
+// the partial's write) weigh on half the bytes (c2 over e4m3: +7 %).  GQA:
+// items already cover several query heads per K/V read, and long partitions
+// (2048 tokens) measured best while the batch alone gives the grid enough
+// items; a batch with fewer unsplit items than three per CTA of the grid
+// (two CTAs on each of GB300's 152 SMs) is cut finer, to about sixteen items
+// per SM at the table's capacity (the lengths themselves are on the device),
+// between 256 and 2048 tokens.  On 256 requests over contexts U[128, 2048]
+// the 2048-token split left a third of the SM time idle in the grid's tail;
+// 256 tokens were 1.28x faster.
+constexpr long long kGridCtas = 2 * 152;
+int resolve_partition(int max_blocks, int bs, int partition_size, int G, bool fp8, int num_seqs,
+                      int num_kv_heads) {
   const int max_ctx = max_blocks * bs;
   if (partition_size < 0) return max_ctx;
-  int P = partition_size > 0 ? partition_size : (G >= 2 ? 2048 : fp8 ? 512 : 256);
+  int P = partition_size;
+  if (P <= 0) {
+    if (G < 2) {
+      P = fp8 ? 512 : 256;
+    } else {
+      const long long items = (long long)num_seqs * ((num_kv_heads + 3) / 4);   // one partition each
+      P = 2048;
+      if (items < 3 * kGridCtas) {
+        const long long want = (long long)max_ctx * items / (8 * kGridCtas);
+        P = 256;
+        while (P < 2048 && 2LL * P <= want) P *= 2;
+      }
+    }
+  }
   if (P >= max_ctx) P = max_ctx;
   return P;
 }
@@ -176,11 +198,12 @@ using namespace pa;
 
 static int partition_size_impl(bool fp8, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                               int max_blocks_per_seq, int block_size, int partition_size) {
-  (void)num_seqs; (void)head_dim;
-  if (max_blocks_per_seq <= 0 || !supported_block_size(block_size)) return PA_ERR_SHAPE;
+  (void)head_dim;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || !supported_block_size(block_size)) return PA_ERR_SHAPE;
   if (partition_size > 0 && partition_size % block_size) return PA_ERR_SHAPE;
   if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return PA_ERR_SHAPE;
-  return resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads, fp8);
+  return resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads, fp8, num_seqs,
+                           num_kv_heads);
 }
 
 extern "C" int pa_decode_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
@@ -231,7 +254,7 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   if (fp8 && (!aligned16(k_scale) || !aligned16(v_scale))) return PA_ERR_ALIGN;
 
   const int P = resolve_partition(max_blocks_per_seq, block_size, partition_size, num_heads / num_kv_heads,
-                                  kv == PA_FP8_E4M3);
+                                  kv == PA_FP8_E4M3, num_seqs, num_kv_heads);
   const long long max_ctx = (long long)max_blocks_per_seq * block_size;
   const int max_parts = (int)((max_ctx + P - 1) / P);
   const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,

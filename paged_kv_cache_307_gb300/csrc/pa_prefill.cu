@@ -76,6 +76,7 @@ struct PrefillParams {
   const int32_t* context_lens;
   const int32_t* query_start;   // ragged batch: [B+1] cumulative query counts; null: Tq each
   int B, Tq, Hq, Hkv, G, QP, n_qt;
+  int rows;                     // ragged batch: total query rows
   int max_blocks, bs, num_blocks;
   float qscale;
 };
@@ -103,6 +104,13 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
   uint32_t y;
   asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+
+// Query rows of sequence i in a ragged batch, or -1 when its pair of
+// starts is decreasing or leaves [0, rows] (flagged; the sequence is skipped).
+__device__ __forceinline__ int seq_queries(const PrefillParams& p, int i) {
+  const int a = __ldg(&p.query_start[i]), b = __ldg(&p.query_start[i + 1]);
+  return (a >= 0 && b >= a && b <= p.rows) ? b - a : -1;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -147,7 +155,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     const int b0 = min(p.B, (int)threadIdx.x * per), b1 = min(p.B, b0 + per);
     int sum = 0;
     for (int i = b0; i < b1; ++i) {
-      const int n = __ldg(&p.query_start[i + 1]) - __ldg(&p.query_start[i]);
+      const int n = seq_queries(p, i);
+      if (n < 0 && blockIdx.x == 0) atomicOr(&g_status_prefill, PA_DEV_BAD_LEN);
       sum += n > 0 ? (n + p.QP - 1) / p.QP : 0;
     }
     int incl = sum;
@@ -162,7 +171,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     for (int w = 0; w < warp; ++w) run += wsum[w];
     for (int i = b0; i < b1; ++i) {
       tpre[i] = run;
-      const int n = __ldg(&p.query_start[i + 1]) - __ldg(&p.query_start[i]);
+      const int n = seq_queries(p, i);
       run += n > 0 ? (n + p.QP - 1) / p.QP : 0;
     }
     if (threadIdx.x == kThreads - 1) tpre[p.B] = run;
@@ -180,11 +189,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     const int ntb = tpre[b + 1] - tpre[b];
     qt = ntb - 1 - (t - tpre[b]);                   // the sequence's longest tile first
     qrow0 = __ldg(&p.query_start[b]);
-    nq = __ldg(&p.query_start[b + 1]) - qrow0;
-    if (nq < 0) {                                   // decreasing starts: flagged, nothing written
-      if (threadIdx.x == 0) atomicOr(&g_status_prefill, PA_DEV_BAD_LEN);
-      return;
-    }
+    nq = seq_queries(p, b);                         // > 0: b holds a tile (bad pairs hold none)
   }
   const int q0 = qt * p.QP;
   int L = __ldg(&p.context_lens[b]);
@@ -550,6 +555,7 @@ static int prefill_impl(void* out, const void* query, const int32_t* query_start
   prm.G = G;
   prm.QP = QP;
   prm.n_qt = (num_queries + QP - 1) / QP;
+  prm.rows = rows;
   prm.max_blocks = max_blocks_per_seq;
   prm.bs = block_size;
   prm.num_blocks = num_blocks;

@@ -341,14 +341,17 @@ def prefill_case(small=False, device="cpu", seed=None, prompts=None, Tq=512, pre
 
 
 def mixed_case(small=False, device="cpu", seed=None, n_decode=None, n_prefill=None, chunk=512, prefix=1024,
-               decode_lens=("uniform", 128, 2048), nan_fill=True):
+               decode_lens=("uniform", 128, 2048), nan_fill=True, heads=None, decode_queries=1):
     """One mixed round ([OS] §8.1–8.2): ``n_prefill`` prompts each running a
     ``chunk``-token prefill chunk at the end of a ``prefix``-token context,
     and ``n_decode`` requests each decoding one token over a context drawn
     from ``decode_lens``; every query's K/V already in the pool.  Queries
     are packed [rows, Hq, D] in sequence order (prefill chunks first) with
-    ``query_start`` [B+1].  c5 shapes (GQA 32/8, D 128, bs 16)."""
-    spec = SPECS["c5"]
+    ``query_start`` [B+1].  c5 shapes (GQA 32/8, D 128, bs 16) unless
+    ``heads`` = (Hq, Hkv) says otherwise; ``decode_queries`` query positions
+    per decode request (1: plain decode; more: a short causal run, as a
+    speculative step would have)."""
+    spec = SPECS["c5"] if heads is None else replace(SPECS["c5"], Hq=heads[0], Hkv=heads[1])
     seed = (spec.seed if seed is None else seed) + 300
     rng = np.random.default_rng(seed)
     n_prefill = (2 if small else 8) if n_prefill is None else n_prefill
@@ -356,7 +359,7 @@ def mixed_case(small=False, device="cpu", seed=None, n_decode=None, n_prefill=No
     _, lo, hi = decode_lens
     dl = rng.integers(lo, hi + 1, size=n_decode)
     lens = np.concatenate([np.full(n_prefill, prefix, dtype=np.int64), dl.astype(np.int64)])
-    nq = np.concatenate([np.full(n_prefill, chunk, dtype=np.int64), np.ones(n_decode, dtype=np.int64)])
+    nq = np.concatenate([np.full(n_prefill, chunk, dtype=np.int64), np.full(n_decode, decode_queries, dtype=np.int64)])
     qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
     bs = spec.bs
     tables, NB, _ = _tables(lens, bs, 0, spec.spare, rng)

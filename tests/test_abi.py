@@ -37,10 +37,17 @@ def test_workspace_and_partition_arithmetic(pa):
     assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, -1) == 0          # never split
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 0) == 12                   # fits one partition
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 6) == -2                   # not a block multiple
-    # e4m3 pools: 512-token partitions for MHA, the same 2048 for grouped queries
+    # e4m3 pools: 512-token partitions for MHA, the grouped-query rule of pa_decode
     assert pa.partition_size(64, 32, 32, 128, 128, 16, 0, fp8=True) == 512
-    assert pa.partition_size(64, 32, 8, 128, 128, 16, 0, fp8=True) == 2048
-    assert pa.partition_size(64, 32, 8, 128, 128, 16, 0) == 2048
+    # grouped queries: 2048 while the batch gives >= 912 unsplit items
+    # (num_seqs * ceil(Hkv / 4)), else finer: 2048 * 128 items / 2432 = 107 -> 256
+    assert pa.partition_size(64, 32, 8, 128, 128, 16, 0, fp8=True) == 256
+    assert pa.partition_size(64, 32, 8, 128, 128, 16, 0) == 256
+    assert pa.partition_size(456, 32, 8, 128, 128, 16, 0) == 2048               # 912 items
+    assert pa.partition_size(455, 32, 8, 128, 128, 16, 0) == 512                # 2048 * 910 / 2432 = 766
+    assert pa.partition_size(256, 32, 8, 128, 2048, 16, 0) == 2048             # 32768 * 512 / 2432 = 6898
+    assert pa.partition_size(256, 32, 8, 128, 80, 16, 0) == 256                # 1280 * 512 / 2432 = 269
+    assert pa.partition_size(512, 32, 8, 128, 81, 16, 0) == 1296               # 1024 items: no split
     assert pa.partition_size(64, 32, 32, 128, 128, 16, 64, fp8=True) == 64
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 0, fp8=True) == 12
     # shared-prefix decode: per (sequence, head) slots for ceil(max_ctx / 256) + 1

@@ -140,7 +140,7 @@ def test_mixed_round_small(pa):
     assert_close(f64(out)[rows], ref, "bf16")
 
 
-@pytest.mark.parametrize("chunk", [1, 31, 32, 33, 100])
+@pytest.mark.parametrize("chunk", [1, 2, 3, 31, 32, 33, 100])
 def test_mixed_round_ragged_chunks_and_empty_sequences(pa, chunk):
     case = W.mixed_case(small=True, device="cuda", chunk=chunk, prefix=300, n_decode=5, n_prefill=3)
     # give sequence 1 no work this round: drop its rows from the packing
@@ -154,6 +154,42 @@ def test_mixed_round_ragged_chunks_and_empty_sequences(pa, chunk):
     out = _run_varlen(pa, case)
     assert pa.last_error() == 0
     assert_close(f64(out)[rows], ref, "bf16")
+
+
+@pytest.mark.parametrize("heads,dq", [((16, 8), 1), ((16, 8), 3), ((16, 8), 4), ((16, 8), 5), ((8, 8), 8), ((32, 4), 1),
+                                      ((32, 8), 2)])
+def test_short_requests_in_a_round(pa, heads, dq):
+    """Requests with a few query positions each (a decode step, or a short
+    causal run such as a speculative step) beside prefill chunks, for several
+    group sizes: every row sees its own causal limit."""
+    case = W.mixed_case(small=True, device="cuda", heads=heads, decode_queries=dq, n_prefill=2, chunk=40,
+                        prefix=200, n_decode=7, decode_lens=("uniform", 1, 300))
+    ref, rows = _oracle_varlen(case)
+    out = _run_varlen(pa, case)
+    assert pa.last_error() == 0
+    assert_close(f64(out)[rows], ref, "bf16")
+
+
+@pytest.mark.parametrize("kind", ["decreasing", "past_the_rows"])
+def test_bad_query_start_is_flagged_and_skipped(pa, kind):
+    """A decreasing pair of starts, or a start past the query rows, is
+    flagged PA_DEV_BAD_LEN and those sequences write nothing; the others
+    are unaffected."""
+    case = W.mixed_case(small=True, device="cuda", n_prefill=3, chunk=40, prefix=200, n_decode=6)
+    qs = case["query_start"].cpu().numpy().astype(np.int64)
+    B = len(qs) - 1
+    ok_seqs = [0] + list(range(4, B - 1))
+    if kind == "decreasing":
+        qs[2] = qs[3] + 1                     # sequence 2 decreasing; 1 and 3 overlap it
+    else:
+        qs[B] = qs[B - 1] + case["q"].shape[0]   # the last sequence ends past the rows
+        ok_seqs = [0, 1, 2, 3] + ok_seqs[1:]
+    case["query_start"] = torch.from_numpy(qs.astype(np.int32)).cuda()
+    out = _run_varlen(pa, case)
+    assert pa.last_error() & pa.DEV_BAD_LEN
+    ref, rows = _oracle_varlen(case, ok_seqs)
+    assert_close(f64(out)[rows], ref, "bf16")
+    assert pa.last_error() == 0
 
 
 def test_uniform_round_equals_fixed_count_tile(pa):
