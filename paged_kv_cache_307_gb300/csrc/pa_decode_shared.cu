@@ -65,6 +65,7 @@ constexpr int kSMaxSeqs = 1024;              // sequences per call on this path
 constexpr int kSMaxGroups = 1024;            // groups per call on this path
 constexpr float kLog2eS = 1.4426950408889634f;
 constexpr uint32_t kAlign = 1024;
+constexpr int kQ = 4;                        // item queue slots (producer -> consumers)
 
 struct SParams {
   void* out;
@@ -76,6 +77,7 @@ struct SParams {
   float* ws_ml;                 // [B*Hq*max_parts][2]  (m in log2 units, l)
   float* ws_o;                  // [B*Hq*max_parts][D]
   int32_t* ws_parts;            // [B] partitions of each sequence (shared + tail)
+  int32_t* ws_next;             // item counter, zero at launch (the host clears it)
   int B, Hq, Hkv, G, ng;
   int max_blocks, bs, num_blocks;
   int ps_blocks;                // shared partition, blocks
@@ -89,12 +91,14 @@ struct SParams {
 // Shared-memory tables every CTA builds (ngE = effective number of groups).
 struct Tables {
   int* Ls;      // [B]      clamped context lengths
-  int* preT;    // [B+1]    prefix of tail items per sequence
-  int* preG;    // [ngE+1]  prefix of items per group (shared + tails)
+  int* preB;    // [B+1]    prefix of tail items per sequence, big tails only
+  int* preM;    // [B+1]    prefix of tail items per sequence, the other tails
+  int* preS;    // [ngE+1]  prefix of shared items per group
   int* shc;     // [ngE]    shared items per group
   int* Sg;      // [ngE]    shared blocks used per group
   int* gsm;     // [ngE+1]  group boundaries
   int ngE;
+  int nB, nS;   // big tail items, shared items (the other tail items follow)
 };
 
 struct SItem {
@@ -190,7 +194,12 @@ __device__ int build_tables(const SParams& p, Tables& t, int* wsum) {
   t.ngE = valid ? p.ng : p.B;
   for (int g = threadIdx.x; g <= t.ngE; g += NTH) t.gsm[g] = valid ? __ldg(&p.group_start[g]) : g;
   __syncthreads();
+  // Items are handed out in three classes, the larger first, so the last
+  // ones to start are short: tail items larger than a full shared item
+  // (shared_items_per_part's usual two KV heads x ps_blocks blocks), the
+  // shared items, then the other tail items.
   const int ipt = part_items(p, p.G, false);
+  const int big_tokens = p.ps_blocks * p.bs * 2 / 4;   // a tail item covers 4 KV heads
   for (int g = threadIdx.x; g < t.ngE; g += NTH) {
     const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
     int S = 0;
@@ -201,36 +210,58 @@ __device__ int build_tables(const SParams& p, Tables& t, int* wsum) {
     t.Sg[g] = S;
     const int nspg = S > 0 ? ceil_div(S, p.ps_blocks) : 0;
     t.shc[g] = nspg * part_items(p, (s1 - s0) * p.G, true);
-    int tsum = 0;
+    t.preS[g] = t.shc[g];
     for (int b = s0; b < s1; ++b) {
       int nsp, ntp;
       seq_parts(p, S, t.Ls[b], nsp, ntp);
-      t.preT[b] = ntp * ipt;
-      tsum += ntp * ipt;
+      const bool big = min(t.Ls[b] - S * p.bs, p.pt_tokens) > big_tokens;
+      t.preB[b] = big ? ntp * ipt : 0;
+      t.preM[b] = big ? 0 : ntp * ipt;
       if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
     }
-    t.preG[g] = t.shc[g] + tsum;
   }
   __syncthreads();
-  block_scan<NTH>(t.preT, p.B, wsum);
-  block_scan<NTH>(t.preG, t.ngE, wsum);
-  return t.preG[t.ngE];
+  block_scan<NTH>(t.preB, p.B, wsum);
+  block_scan<NTH>(t.preM, p.B, wsum);
+  block_scan<NTH>(t.preS, t.ngE, wsum);
+  t.nB = t.preB[p.B];
+  t.nS = t.preS[t.ngE];
+  return t.nB + t.nS + t.preM[p.B];
 }
 
-// Item i -> its description (every role computes the same).
-__device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i, SItem& it) {
-  int lo = 0, hi = t.ngE - 1;           // last group whose first item is <= i
+// Largest index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x):
+// over a prefix of item counts, the entry that holds item x.
+__device__ __forceinline__ int last_le(const int* a, int n, int x) {
+  int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (t.preG[mid] <= i) lo = mid;
+    if (a[mid] <= x) lo = mid;
     else hi = mid - 1;
   }
-  const int g = lo;
-  const int r = i - t.preG[g];
+  return lo;
+}
+
+// Item i -> its description (every role computes the same): big tail
+// items [0, nB), shared items [nB, nB + nS), the other tail items after.
+__device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i, SItem& it) {
+  int g, r, b = 0, rr = 0;
+  const bool shared = i >= t.nB && i < t.nB + t.nS;
+  if (shared) {
+    r = i - t.nB;
+    g = last_le(t.preS, t.ngE, r);      // the group holding shared item r
+    r -= t.preS[g];
+  } else {
+    const int* pre = i < t.nB ? t.preB : t.preM;
+    const int k = i < t.nB ? i : i - t.nB - t.nS;
+    b = last_le(pre, p.B, k);           // the sequence holding tail item k
+    rr = k - pre[b];
+    g = last_le(t.gsm, t.ngE, b);       // its group
+    r = 0;
+  }
   const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
   const int S = t.Sg[g];
   it.S = S;
-  if (r < t.shc[g]) {
+  if (shared) {
     const int R = (s1 - s0) * p.G;
     int nhg, chunks;
     if (R <= 16) {
@@ -260,15 +291,7 @@ __device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i,
     it.shared = 1;
     it.s1 = s1;
   } else {
-    const int r2 = r - t.shc[g] + t.preT[s0];
-    int blo = s0, bhi = s1 - 1;         // last member whose first tail item is <= r2
-    while (blo < bhi) {
-      const int mid = (blo + bhi + 1) >> 1;
-      if (t.preT[mid] <= r2) blo = mid;
-      else bhi = mid - 1;
-    }
-    const int b = blo;
-    const int rr = r2 - t.preT[b];
+    (void)r;
     const int nhg = ceil_div(p.Hkv, 4);
     const int part = rr / nhg;
     it.kvh0 = (rr - part * nhg) * 4;
@@ -616,15 +639,19 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   unsigned char* tilesV = smem + (size_t)p.nstage * stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(tilesV + (size_t)p.nstage * stage_bytes);
   uint64_t* empty = full + p.nstage;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.nstage);
-  int* wsum = const_cast<int*>(abort_flag) + 4;      // [8]
+  uint64_t* qfull = empty + p.nstage;                 // [kQ] item queue: index written
+  uint64_t* qempty = qfull + kQ;                      // [kQ] item queue: index read by every consumer
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + kQ);
+  int* qid = const_cast<int*>(abort_flag) + 4;        // [kQ]
+  int* wsum = qid + kQ;                               // [8]
   const int ngMax = max(p.ng, p.B);
   Tables t;
   t.Ls = wsum + 8;
-  t.preT = t.Ls + p.B;
-  t.gsm = t.preT + p.B + 1;
-  t.preG = t.gsm + ngMax + 1;
-  t.shc = t.preG + ngMax + 1;
+  t.preB = t.Ls + p.B;
+  t.preM = t.preB + p.B + 1;
+  t.gsm = t.preM + p.B + 1;
+  t.preS = t.gsm + ngMax + 1;
+  t.shc = t.preS + ngMax + 1;
   t.Sg = t.shc + ngMax;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -632,6 +659,10 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
     for (int s = 0; s < p.nstage; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSW);
+    }
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], kSW);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -652,7 +683,27 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
     uint32_t st_ph = 0;
     uint32_t ucount = 0;                           // stages walked so far
     uint32_t armed_end = 0;                        // 1 + index of the last stage armed
-    for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    // Items are taken from the launch-wide counter as this CTA gets to them
+    // (the next index is fetched while the current item's loads go out) and
+    // passed to the consumers through a queue of kQ slots.
+    int pend = 0;
+    if (lane == 0) pend = atomicAdd(p.ws_next, 1);
+    for (int kq = 0;; ++kq) {
+      const int q = kq % kQ;
+      int v = -1;
+      if (lane == 0) {
+        if (!*abort_flag && mbar_wait(&qempty[q], ((uint32_t)(kq / kQ) & 1u) ^ 1u)) {
+          v = pend < n_items ? pend : -1;
+          if (v >= 0) pend = atomicAdd(p.ws_next, 1);
+          qid[q] = v;
+          mbar_arrive(&qfull[q]);
+        } else if (!*abort_flag) {
+          atomicOr(&g_status_shared, PA_DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+      v = __shfl_sync(0xffffffffu, v, 0);
+      if (v < 0) break;
       SItem it;
       s_item(p, t, v, it);
       const int32_t* row = p.block_tables + (size_t)it.s0 * p.max_blocks;
@@ -730,7 +781,23 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   // -------------------------------------------------------------- consumers
   int st_idx = 0;
   uint32_t st_ph = 0;
-  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+  for (int kq = 0;; ++kq) {
+    const int q = kq % kQ;
+    bool live = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+    if (live) {
+      const bool late = !mbar_wait(&qfull[q], (uint32_t)(kq / kQ) & 1u);
+      if (__any_sync(0xffffffffu, late)) {
+        live = false;
+        if (lane == 0) {
+          atomicOr(&g_status_shared, PA_DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+    }
+    const int v = live ? qid[q] : -1;
+    __syncwarp();
+    if (live && lane == 0) mbar_arrive(&qempty[q]);
+    if (v < 0) break;
     SItem it;
     s_item(p, t, v, it);
     const int hd = warp / it.wh;
@@ -879,7 +946,7 @@ SharedPlan shared_plan(int num_seqs, int num_heads, int num_kv_heads, int head_d
   // a sequence has at most ceil(x / Ps) + ceil((max_ctx - x) / Pt) partitions
   pl.max_parts = (max_ctx + minp - 1) / minp + 1;
   const size_t rows = (size_t)num_seqs * num_heads * pl.max_parts;
-  pl.parts_bytes = ((size_t)num_seqs * 4 + 255) / 256 * 256;
+  pl.parts_bytes = ((size_t)(num_seqs + 1) * 4 + 255) / 256 * 256;   // + the item counter
   pl.ml_bytes = (rows * 8 + 255) / 256 * 256;
   pl.o_bytes = rows * head_dim * 4;
   return pl;
@@ -958,6 +1025,7 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   prm.shared_blocks = shared_blocks;
   char* ws = static_cast<char*>(workspace);
   prm.ws_parts = reinterpret_cast<int32_t*>(ws);
+  prm.ws_next = prm.ws_parts + num_seqs;
   prm.ws_ml = reinterpret_cast<float*>(ws + pl.parts_bytes);
   prm.ws_o = reinterpret_cast<float*>(ws + pl.parts_bytes + pl.ml_bytes);
   prm.B = num_seqs;
@@ -978,11 +1046,12 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   // the tables for two CTAs per SM (2..6), or, when a stage is so large that
   // two do not fit, one CTA per SM with up to 3.
   // shared memory: stages (K and V tiles), their two mbarriers each, the
-  // abort flag (16 bytes), then the tables: wsum[8], Ls[B], preT[B+1],
-  // gsm[ngMax+1], preG[ngMax+1], shc[ngMax], Sg[ngMax]
+  // item queue's 2 x kQ mbarriers, the abort flag (16 bytes), qid[kQ], then
+  // the tables: wsum[8], Ls[B], preB[B+1], preM[B+1], gsm[ngMax+1],
+  // preS[ngMax+1], shc[ngMax], Sg[ngMax]
   const size_t stage = 2 * (size_t)kTiles * prm.tile_bytes;
   const size_t ngMax = (size_t)(num_groups > num_seqs ? num_groups : num_seqs);
-  const size_t tables = 16 + 4 * (8 + 2 * (size_t)num_seqs + 1 + 4 * ngMax + 2);
+  const size_t tables = 2 * kQ * sizeof(uint64_t) + 16 + 4 * (kQ + 8 + 3 * (size_t)num_seqs + 2 + 4 * ngMax + 2);
   const size_t per_cta = (227 * 1024) / 2 - 1024;
   int ns = (int)((per_cta - tables - kAlign) / (stage + 16));
   if (ns >= 2) {
@@ -1002,6 +1071,8 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   const int occ = shared_occupancy(kern, smem, dev);
   if (occ <= 0) return PA_ERR_CUDA;
   const unsigned grid = (unsigned)(occ * device_sm_count());
+  if (!ck(cudaMemsetAsync(prm.ws_next, 0, sizeof(int32_t), (cudaStream_t)stream), "cudaMemsetAsync(item counter)"))
+    return PA_ERR_CUDA;
   void* args[] = {&mapK, &mapV, &prm};
   if (!ck(cudaLaunchKernel(kern, dim3(grid), dim3(kST), args, smem, (cudaStream_t)stream),
           "cudaLaunchKernel(shared_decode_kernel)"))

@@ -53,7 +53,8 @@ def test_workspace_and_partition_arithmetic(pa):
     # shared-prefix decode: per (sequence, head) slots for ceil(max_ctx / 256) + 1
     # partitions, a partition count per sequence, never less than pa_decode's
     rows = 512 * 32 * (1280 // 256 + 1)
-    assert pa.shared_workspace_bytes(512, 32, 8, 128, 80, 16, 0, 64) == 2048 + rows * 8 + rows * 128 * 4
+    # partition counts (B ints) and the item counter, rounded to 256 bytes: (512 + 1) * 4 -> 2304
+    assert pa.shared_workspace_bytes(512, 32, 8, 128, 80, 16, 0, 64) == 2304 + rows * 8 + rows * 128 * 4
     assert pa.shared_workspace_bytes(64, 32, 32, 128, 128, 16, 0, 8) >= pa.workspace_bytes(64, 32, 32, 128, 128, 16)
     # shapes the shared path does not take fall back to pa_decode's workspace
     assert pa.shared_workspace_bytes(4, 256, 4, 128, 80, 16, 0, 1) == pa.workspace_bytes(4, 256, 4, 128, 80, 16, 0)
