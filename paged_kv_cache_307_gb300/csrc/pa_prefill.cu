@@ -103,6 +103,26 @@ __device__ __forceinline__ float ex2_f32(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed fp32 pairs (one 64-bit register, the f32x2 instructions: two
+// lanes of fma or add per instruction, each rounded as the scalar one).
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 // max(a, b, c) in one instruction (the three-input form of max.f32).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -423,27 +443,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       // 32h + 2c + 1).  The row sum adds the fp32 exponentials; P carries
       // their bf16 rounding (a relative 2^-9 per term, unbiased).
       const float negm = m_ref == -INFINITY ? 0.f : -m_ref;   // all-masked rows: every s is -inf
-      float ls8[8];
+      const uint64_t qs2 = f2pack(p.qscale, p.qscale), nm2 = f2pack(negm, negm);
+      uint64_t ls2[4];                               // eight partial row sums, as four pairs
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
+      for (int i = 0; i < 4; ++i) ls2[i] = f2pack(0.f, 0.f);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pw[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          // exponents and 2^x in fp32, then one bf16 pair for the product
-          // (two MUFU operations a pair: fewer instructions than an f16 pair
-          // widened back for the sum, 819 -> 848 TFLOP/s on the c5 tile)
-          float2 pf;
-          pf.x = ex2_f32(fmaf(__uint_as_float(v[hf][2 * c]), p.qscale, negm));
-          pf.y = ex2_f32(fmaf(__uint_as_float(v[hf][2 * c + 1]), p.qscale, negm));
-          const __nv_bfloat162 pk = __floats2bfloat162_rn(pf.x, pf.y);
-          ls8[(2 * c) & 7] += pf.x;
-          ls8[(2 * c + 1) & 7] += pf.y;
+          // exponents as one packed fp32 fma per pair, 2^x in fp32, one bf16
+          // pair for the product, one packed add into the sums
+          float x0, x1;
+          f2unpack(ffma2(f2pack(__uint_as_float(v[hf][2 * c]), __uint_as_float(v[hf][2 * c + 1])), qs2, nm2), x0,
+                   x1);
+          const float p0 = ex2_f32(x0), p1 = ex2_f32(x1);
+          const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+          ls2[c & 3] = fadd2(ls2[c & 3], f2pack(p0, p1));
           pw[c] = *reinterpret_cast<const uint32_t*>(&pk);
         }
         tmem_st16(tmem + st * kKT + hf * 16 + lane_off, pw);
       }
+      float ls8[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f2unpack(ls2[i], ls8[2 * i], ls8[2 * i + 1]);
       lsum += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       tmem_st_wait();
       tc_fence_before();
