@@ -242,7 +242,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
+    if (nt > 0) {
+      // Q goes out at once (this thread is also the K producer's lane 0):
+      // its latency overlaps the TMEM allocation and the CTA barrier.
+      // Q as [rows, Hq, D]: rows past the sequence's queries (a ragged tile)
+      // belong to the next sequence or are zero-filled past the end; their
+      // scores are computed and never written.
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapK);
+      mbar_arrive_expect_tx(&bars->q, 2 * kQHalf);
+      const uint64_t pol = policy_evict_first();
+      tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, qrow0 + q0, 0, pol);
+      tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, qrow0 + q0, 0, pol);
+    }
   }
+  // the producers' first block-table entries, read before the CTA barrier
+  int blk_first = 0;
+  if ((warp == 0 || warp == 6) && nt > 0 && lane < min(kKT / p.bs, (L + p.bs - 1) / p.bs))
+    blk_first = __ldg(&p.block_tables[(size_t)b * p.max_blocks + lane]);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -261,22 +278,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     const bool is_k = warp == 0;
     int issued_q = 0, issued = 0;
     if (nt > 0) {
-      if (lane == 0) {
-        if (is_k) {
-          prefetch_tensormap(&mapQ);
-          prefetch_tensormap(&mapK);
-          mbar_arrive_expect_tx(&bars->q, 2 * kQHalf);
-          const uint64_t pol = policy_evict_first();
-          // Q as [rows, Hq, D]: rows past the sequence's queries (a ragged
-          // tile) belong to the next sequence or are zero-filled past the
-          // end; their scores are computed and never written.
-          tma_load_4d(smem + kOffQ, &mapQ, &bars->q, 0, kvh * p.G, qrow0 + q0, 0, pol);
-          tma_load_4d(smem + kOffQ + kQHalf, &mapQ, &bars->q, 64, kvh * p.G, qrow0 + q0, 0, pol);
-        } else {
-          prefetch_tensormap(&mapV);
-        }
-      }
-      issued_q = is_k ? 1 : 0;
+      if (lane == 0 && !is_k) prefetch_tensormap(&mapV);
+      issued_q = is_k ? 1 : 0;                    // Q went out with the barriers (above)
       const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by other query tiles
       const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
       const int nbt = kKT / p.bs;
@@ -292,7 +295,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         const int nvalid = min(nbt, (L - k0 + p.bs - 1) / p.bs);
         int blk = 0;
         if (lane < nvalid) {
-          blk = __ldg(&row[k0 / p.bs + lane]);
+          blk = t == 0 ? blk_first : __ldg(&row[k0 / p.bs + lane]);
           if ((unsigned)blk >= (unsigned)p.num_blocks) {
             if (is_k) atomicOr(&g_status_prefill, PA_DEV_BAD_BLOCK);
             blk = 0;
