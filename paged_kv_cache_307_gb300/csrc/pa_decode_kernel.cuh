@@ -207,6 +207,9 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the merge kernel (a programmatic dependent on eager calls) may be
+  // scheduled now; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1335,6 +1338,10 @@ merge_kernel(const DecodeParams p) {
   if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;
   const int nparts = L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
   if (nparts <= 1) return;
+  // launched as a programmatic dependent of the decode kernel (eager calls):
+  // the partials are read only once that grid has completed and its writes
+  // are visible; a plain launch passes straight through
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const size_t base = (size_t)gw * p.max_parts;
   float M = -INFINITY;
   for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[(base + i) * 2]);
