@@ -20,6 +20,25 @@ bool ck(cudaError_t e, const char* what) {
   return false;
 }
 
+cudaError_t launch_after(const void* kernel, dim3 grid, dim3 block, void** args, cudaStream_t stream) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();      // not accepted here: a plain launch
+  }
+  return cudaLaunchKernel(kernel, grid, block, args, 0, stream);
+}
+
 bool raise_smem_limit(const void* kernel, int dev) {
   static std::mutex mu;
   static std::set<std::pair<const void*, int>> done;

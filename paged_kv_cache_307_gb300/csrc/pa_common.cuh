@@ -225,6 +225,14 @@ bool ck(cudaError_t e, const char* what);
 // maximum (once per kernel and device).
 bool raise_smem_limit(const void* kernel, int dev);
 
+// Launch `kernel` on `stream` as a programmatic dependent of the kernel before
+// it (it may be scheduled once that grid has started; it must wait with
+// griddepcontrol.wait before reading that grid's results), unless the stream
+// is being captured, where a plain launch is kept (graph replay measured
+// slower with the programmatic edge).  Falls back to a plain launch when the
+// runtime does not accept the attribute.
+cudaError_t launch_after(const void* kernel, dim3 grid, dim3 block, void** args, cudaStream_t stream);
+
 // Per-translation-unit status fetch (returns the sticky word and clears it).
 unsigned fetch_status_cache_ops();
 unsigned fetch_status_decode();

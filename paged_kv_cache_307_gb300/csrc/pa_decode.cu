@@ -357,28 +357,10 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
     const long long warps = (long long)num_seqs * num_heads;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     void* margs[] = {&prm};
-    // Eager calls launch the merge as a programmatic dependent of the decode
-    // kernel, so its CTAs are resident when the decode grid completes (c2
-    // +0.9 %); under stream capture the plain launch is kept (graph replay
-    // measured 2-3 % slower with the programmatic edge).
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    bool launched = false;
-    if (cudaStreamIsCapturing((cudaStream_t)stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(blocks);
-      cfg.blockDim = dim3(256);
-      cfg.dynamicSmemBytes = 0;
-      cfg.stream = (cudaStream_t)stream;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr.val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      launched = cudaLaunchKernelExC(&cfg, L.merge, margs) == cudaSuccess;
-      if (!launched) (void)cudaGetLastError();    // not accepted here: a plain launch below
-    }
-    if (!launched && !ck(cudaLaunchKernel(L.merge, dim3(blocks), dim3(256), margs, 0, (cudaStream_t)stream),
-                         "cudaLaunchKernel(merge_kernel)"))
+    // eager calls: the merge as a programmatic dependent of the decode kernel,
+    // so its CTAs are resident when the decode grid completes (c2 +0.9 %)
+    if (!ck(launch_after(L.merge, dim3(blocks), dim3(256), margs, (cudaStream_t)stream),
+            "cudaLaunchKernel(merge_kernel)"))
       return PA_ERR_CUDA;
   }
   return PA_OK;

@@ -655,6 +655,9 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   t.Sg = t.shc + ngMax;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the merge kernel (a programmatic dependent on eager calls) may be
+  // scheduled now; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.nstage; ++s) {
       mbar_init(&full[s], 1);
@@ -820,6 +823,9 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= (long long)p.B * p.Hq) return;
+  // a programmatic dependent of the decode kernel on eager calls: the
+  // partition counts and partials are read once that grid has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = (int)(gw / p.Hq);
   const int nparts = p.ws_parts[b];
   if (nparts <= 1) return;
@@ -1080,7 +1086,7 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   const long long warps = (long long)num_seqs * num_heads;
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
   void* margs[] = {&prm};
-  if (!ck(cudaLaunchKernel(merge, dim3(blocks), dim3(256), margs, 0, (cudaStream_t)stream),
+  if (!ck(launch_after(merge, dim3(blocks), dim3(256), margs, (cudaStream_t)stream),
           "cudaLaunchKernel(shared_merge_kernel)"))
     return PA_ERR_CUDA;
   return PA_OK;
