@@ -129,7 +129,10 @@ int pa_reshape_and_cache(const void* key, const void* value,
  *                  split, > 0 = a multiple of block_size.  A sequence longer
  *                  than one partition is processed as independent partitions
  *                  whose (max, sum, unnormalised output) states are merged by
- *                  log-sum-exp in a second kernel.
+ *                  log-sum-exp in a second kernel (outside stream capture it
+ *                  is launched as a programmatic dependent of the first and
+ *                  waits for it on the device; inside a capture, a plain
+ *                  launch).
  *   workspace      device scratch of at least pa_decode_workspace_bytes()
  *                  with the same sizes (may be NULL when that is 0).  Its
  *                  contents on entry do not matter; calls that share one
