@@ -1197,9 +1197,23 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                   EK::unpack(*reinterpret_cast<const uint4*>(kt + t * (HG * ROW) + (li + hf * LPT) * 16),
                              kf + hf * EPC);
   #pragma unroll
-                for (int h = 0; h < GT; ++h)
+                for (int h = 0; h < GT; ++h) {
+                  if constexpr (SCALED) {
+                    // e4m3: scalar FMAs (the widened codes do not pair up in
+                    // registers: the packed form measured 15 % slower)
   #pragma unroll
-                  for (int d = 0; d < DPL; ++d) part[h] = fmaf(q[h][d], kf[d], part[h]);
+                    for (int d = 0; d < DPL; ++d) part[h] = fmaf(q[h][d], kf[d], part[h]);
+                  } else {
+                    // two interleaved partial sums on packed fp32 pairs
+                    uint64_t acc = f2pack(0.f, 0.f);
+  #pragma unroll
+                    for (int d = 0; d < DPL; d += 2)
+                      acc = ffma2(f2pack(q[h][d], q[h][d + 1]), f2pack(kf[d], kf[d + 1]), acc);
+                    float a0, a1;
+                    f2unpack(acc, a0, a1);
+                    part[h] = a0 + a1;
+                  }
+                }
               }
               // e4m3: the token's K scale multiplies its whole score
               float ksc = 1.f;
@@ -1220,8 +1234,17 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
               const float alpha = mx == -INFINITY ? 1.f : exp2f(m[h] - mx);
               m[h] = mx;
               l[h] *= alpha;
+              if constexpr (SCALED) {
   #pragma unroll
-              for (int d = 0; d < DPL; ++d) o[h][d] *= alpha;
+                for (int d = 0; d < DPL; ++d) o[h][d] *= alpha;
+              } else {
+                const uint64_t al2 = f2pack(alpha, alpha);
+  #pragma unroll
+                for (int d = 0; d < DPL; d += 2) {
+                  const uint64_t o2 = fmul2(f2pack(o[h][d], o[h][d + 1]), al2);
+                  f2unpack(o2, o[h][d], o[h][d + 1]);
+                }
+              }
             }
   #pragma unroll
             for (int k = 0; k < NS; ++k) {
@@ -1240,8 +1263,17 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
                   const float pk = exp2f(s[k][h] - m[h]);
                   l[h] += pk;
                   const float pw = SCALED ? pk * vsc : pk;
+                  if constexpr (SCALED) {
   #pragma unroll
-                  for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(pw, vf[d], o[h][d]);
+                    for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(pw, vf[d], o[h][d]);
+                  } else {
+                    const uint64_t pw2 = f2pack(pw, pw);
+  #pragma unroll
+                    for (int d = 0; d < DPL; d += 2) {
+                      const uint64_t o2 = ffma2(pw2, f2pack(vf[d], vf[d + 1]), f2pack(o[h][d], o[h][d + 1]));
+                      f2unpack(o2, o[h][d], o[h][d + 1]);
+                    }
+                  }
                 }
               }
             }
