@@ -284,6 +284,36 @@ def test_permuted_pool_gives_bit_identical_output(pa):
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
+@pytest.mark.parametrize("name,partition", [("c2", 64), ("c4", 64), ("c3", 0)])
+def test_decode_on_a_side_stream_is_bit_identical(pa, name, partition):
+    """Split-K decode enqueued on a user stream (the merge is then a
+    programmatic dependent of the decode kernel) gives the same bits as on
+    the current stream, and back to back calls on that stream do not see
+    each other's partials."""
+    c = _cuda_case(name, small=True)
+    pa.reshape_and_cache(c.key, c.value, c.slot_mapping, c.k_cache, c.v_cache)
+    torch.cuda.synchronize()
+    ref = torch.full_like(c.q, float("nan"))
+    pa.decode(ref, c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale, partition_size=partition)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    ws = pa.alloc_workspace(c.q, c.k_cache, c.block_tables, partition_size=partition)
+    outs = [torch.full_like(c.q, float("nan")) for _ in range(3)]
+    q2 = c.q.flip(0).contiguous()          # a second, different case between two identical ones
+    with torch.cuda.stream(side):
+        pa.decode(outs[0], c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale,
+                  partition_size=partition, workspace=ws, stream=side)
+        pa.decode(outs[1], q2, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale,
+                  partition_size=partition, workspace=ws, stream=side)
+        pa.decode(outs[2], c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale,
+                  partition_size=partition, workspace=ws, stream=side)
+    side.synchronize()
+    assert pa.last_error() == 0
+    assert torch.equal(outs[0].view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(outs[2].view(torch.int16), ref.view(torch.int16))
+    assert_close(f64(ref), oracle_decode(c), "bf16")
+
+
 def test_shared_prefix_equals_private_copies(pa):
     c = _cuda_case("c5", small=True)
     pa.reshape_and_cache(c.key, c.value, c.slot_mapping, c.k_cache, c.v_cache)

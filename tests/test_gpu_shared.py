@@ -226,6 +226,34 @@ def test_shared_graph_replay_is_bit_identical(pa):
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
 
 
+def test_shared_back_to_back_on_a_side_stream(pa):
+    """Three calls in a row on a user stream sharing one workspace (the work
+    counter is cleared before each, the merge waits for its decode kernel on
+    the device): the first and third give the current stream's bits, the
+    middle one (another query batch) its own."""
+    c = _case()
+    ref = _run(pa, c, partition=64)
+    q2 = c.q.flip(0).contiguous()
+    gs, sb = c.extra["group_start"], c.extra["shared_blocks"]
+    ws = pa.alloc_shared_workspace(c.q, c.k_cache, c.block_tables, sb.shape[0], partition_size=64)
+    outs = [torch.full_like(c.q, float("nan")) for _ in range(3)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for o, q in zip(outs, (c.q, q2, c.q)):
+            pa.decode_shared(o, q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, gs, sb, c.scale,
+                             partition_size=64, workspace=ws, stream=side)
+    side.synchronize()
+    assert pa.last_error() == 0
+    assert torch.equal(outs[0].view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(outs[2].view(torch.int16), ref.view(torch.int16))
+    mid = torch.full_like(c.q, float("nan"))
+    pa.decode_shared(mid, q2, c.k_cache, c.v_cache, c.block_tables, c.context_lens, gs, sb, c.scale,
+                     partition_size=64)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[1].view(torch.int16), mid.view(torch.int16))
+
+
 def test_unsupported_shapes_run_plain_decode(pa):
     # fp32 pools and groups of more than 8 query heads take pa_decode's path
     # unchanged
