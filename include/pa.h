@@ -178,7 +178,7 @@ int pa_decode(void* out, const void* query,
  *                  through its own row.  The two attention states are
  *                  merged by log-sum-exp (exact up to rounding: the online
  *                  softmax is associative).
- *   partition_size 0: automatic (256-token partitions of the shared blocks;
+ *   partition_size 0: automatic (512-token partitions of the shared blocks;
  *                  the private tails as pa_decode's automatic choice);
  *                  > 0: a multiple of block_size used for both; < 0: no
  *                  split of either.
