@@ -36,7 +36,8 @@
 //      - CUDA cores (MHA, fp32, e4m3 MHA, odd groups): LPT lanes share one
 //        token, each owning one or two 16-byte chunks of head_dim; scores in
 //        the base-2 domain (q pre-multiplied by scale*log2 e), exp2f, one
-//        online-softmax state per lane group;
+//        online-softmax state per lane group; on 16/32-bit pools the dot
+//        products and the P V update run on packed fp32 pairs (f32x2);
 //      - tensor cores, tokens in M (bf16 and e4m3, groups of up to 8):
 //        S^T = K Q^T with the 16 tokens of a k-step as the M rows and the
 //        heads as N = 8, P^T transposed in registers (movmatrix) into the B
@@ -49,7 +50,9 @@
 //    rounding (the update is associative).
 //  * A sequence whose context fits one partition is normalised and written
 //    directly; longer ones write (m, l, unnormalised o) per partition to the
-//    workspace, and merge_kernel combines them.
+//    workspace, and merge_kernel combines them (on eager calls it is launched
+//    as a programmatic dependent: its CTAs may be resident before this grid
+//    completes, and it waits for it with griddepcontrol.wait).
 //  * Waits are bounded (2 s).  A wait that runs out sets PA_DEV_TIMEOUT and an
 //    abort flag; every role then skips the remaining work while still passing
 //    the CTA's barriers, and the producer waits (bounded) for the TMA loads it

@@ -20,13 +20,16 @@
 //    after the shared blocks, four KV heads) whose rows are the sequence's
 //    query heads.  A shared block is read from HBM once for every row of the
 //    group instead of once per member.
-//  * Items are enumerated densely per CTA (a persistent grid strides over
-//    them): every CTA builds, in shared memory, the clamped lengths, the
-//    per-group shared length S_g = min(shared_blocks[g], floor(L_b / bs)
-//    over the members) and prefix sums of items per group and of tail items
-//    per sequence; a group's shared items come first, then its members'
-//    tails, so CTAs running side by side mix the tensor-core-heavy shared
-//    items with the streaming tail items.
+//  * Every CTA builds, in shared memory, the clamped lengths, the per-group
+//    shared length S_g = min(shared_blocks[g], floor(L_b / bs) over the
+//    members) and prefix sums of items in three classes, handed out in this
+//    order: tail items larger than a full shared item, the shared items
+//    (512-token partitions by default), the other tail items.  A persistent
+//    grid takes items at run time from a counter in the workspace (the host
+//    clears it before each launch): the producer fetches the next index while
+//    the current item's loads go out and passes each index to the consumer
+//    warps through a four-slot queue in shared memory, so a CTA that
+//    finishes early takes the next item instead of idling.
 //  * One producer warp per CTA fills a ring of stages by TMA; a stage holds
 //    four (block, KV head) tiles of K and V (128-byte-swizzled 64-column
 //    spans): four heads of one block, or two heads of two blocks.
@@ -42,7 +45,8 @@
 //    between warps.  A row whose sequence has one partition in all writes
 //    its normalised output; otherwise it writes (max, sum, unnormalised
 //    output) to its partition's slot of the workspace and a merge kernel
-//    combines the slots.
+//    combines the slots (on eager calls launched as a programmatic dependent
+//    that waits for this grid on the device).
 //  * Waits are bounded (2 s) as in pa_decode: a wait that runs out sets
 //    PA_DEV_TIMEOUT, the CTA skips its remaining work and waits (bounded) for
 //    its own TMA loads before it exits.
