@@ -133,9 +133,12 @@ def traffic_record(workload, batch, sources=DECODE_SOURCES):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms from just
+    before the timed region until after it; the summary keeps the samples
+    whose timestamps fall inside the region (begin() .. end()), or, for a
+    region shorter than the sampling interval, the samples nearest to it."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -143,16 +146,23 @@ class ClockSampler:
         self.index = index
         self.lines = []
         self.proc = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(self.index)],
+                                          "-lms", "20", "-i", str(self.index)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
             self.proc = None
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -167,24 +177,37 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            try:
+                rows.append((ts, float(f[2]), float(f[3]),
+                             [n for n, val in zip(names, f[6:10]) if val.lower() == "active"]))
             except ValueError:
                 continue
-            for n, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"error": "no samples in the timed region"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not rows:
+            return {"error": "no samples"}
+        sel, where = rows, "all samples (no region marks)"
+        if self.t0 is not None and self.t1 is not None and all(r[0] is not None for r in rows):
+            inside = [r for r in rows if self.t0 - 0.005 <= r[0] <= self.t1 + 0.005]
+            if inside:
+                sel, where = inside, "inside the timed region"
+            else:
+                mid = 0.5 * (self.t0 + self.t1)
+                near = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+                sel, where = near, "nearest to the timed region (shorter than the 20 ms sampling interval)"
+        reasons = sorted({n for r in sel for n in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel), "which": where,
+                "region_ms": round((self.t1 - self.t0) * 1e3, 2) if self.t0 and self.t1 else None}
 
 
 def pipelined_e2e(stream, host_inputs, out_like, compute, n, warm=3):
@@ -570,11 +593,13 @@ def run_prefill(args, rank, world, local_rank):
                            else local_rank)
     sampler.start()
     time.sleep(0.25)
+    sampler.begin()
     start.record(stream)
     for _ in range(K):
         step()
     stop.record(stream)
     torch.cuda.synchronize()
+    sampler.end()
     clocks = sampler.stop()
     total_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     assert pa.last_error() == 0
@@ -657,11 +682,13 @@ def run_swap(args, rank, world, local_rank):
                            else local_rank)
     sampler.start()
     time.sleep(0.25)
+    sampler.begin()
     e[0].record(stream)
     for _ in range(K):
         step()
     e[1].record(stream)
     torch.cuda.synchronize()
+    sampler.end()
     clocks = sampler.stop()
     assert pa.last_error() == 0
     ms = max_over_ranks(e[0].elapsed_time(e[1]), world, dev) / K
@@ -777,7 +804,9 @@ def run_mixed(args, rank, world, local_rank):
                            else local_rank)
     sampler.start()
     time.sleep(0.25)
+    sampler.begin()
     ms = max_over_ranks(timed(step, K), world, dev)
+    sampler.end()
     clocks = sampler.stop()
     assert pa.last_error() == 0
     split_ms = timed(split_step, K)
@@ -895,6 +924,7 @@ def run_ours(args, rank, world, local_rank):
                            else local_rank)
     sampler.start()
     time.sleep(0.25)
+    sampler.begin()
     start.record(stream)
     for i in range(K):
         append()
@@ -903,6 +933,7 @@ def run_ours(args, rank, world, local_rank):
         d1[i].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
+    sampler.end()
     clocks = sampler.stop()
     if world > 1:
         dist.barrier()
