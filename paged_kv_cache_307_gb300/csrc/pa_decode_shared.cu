@@ -24,7 +24,10 @@
 //    shared length S_g = min(shared_blocks[g], floor(L_b / bs) over the
 //    members) and prefix sums of items in three classes, handed out in this
 //    order: tail items larger than a full shared item, the shared items
-//    (512-token partitions by default), the other tail items.  A persistent
+//    (512-token partitions by default), the other tail items; the tail
+//    items of each class go largest first (a stable counting sort of the
+//    sequences on their tail length), so the last items to start are the
+//    shortest and the CTAs finish close together.  A persistent
 //    grid takes items at run time from a counter in the workspace (the host
 //    clears it before each launch): the producer fetches the next index while
 //    the current item's loads go out and passes each index to the consumer
@@ -70,6 +73,8 @@ constexpr int kSMaxGroups = 1024;            // groups per call on this path
 constexpr float kLog2eS = 1.4426950408889634f;
 constexpr uint32_t kAlign = 1024;
 constexpr int kQ = 4;                        // item queue slots (producer -> consumers)
+constexpr int kKH = 32;                      // tail-size buckets per class (big tails, others)
+constexpr int kLB = 8;                       // lengths loaded per thread per round of global loads
 
 struct SParams {
   void* out;
@@ -90,19 +95,22 @@ struct SParams {
   int nstage;
   uint32_t tile_bytes;          // one (block, head) tile of K (or V): bs * D * 2
   float qscale;                 // scale * log2(e)
+  int bs_shift;                 // log2(bs)
+  int ginv;                     // ceil(2^16 / G): row r (< 1024 G) of a group -> member (r * ginv) >> 16
 };
 
 // Shared-memory tables every CTA builds (ngE = effective number of groups).
 struct Tables {
   int* Ls;      // [B]      clamped context lengths
-  int* preB;    // [B+1]    prefix of tail items per sequence, big tails only
-  int* preM;    // [B+1]    prefix of tail items per sequence, the other tails
+  int* perm;    // [B]      sequences with tail items, largest item first
+  int* preT;    // [B+1]    prefix of tail items over perm's order
   int* preS;    // [ngE+1]  prefix of shared items per group
-  int* shc;     // [ngE]    shared items per group
   int* Sg;      // [ngE]    shared blocks used per group
   int* gsm;     // [ngE+1]  group boundaries
+  unsigned char* one;   // [B] 1: the sequence has one partition in all (its rows store the output)
   int ngE;
-  int nB, nS;   // big tail items, shared items (the other tail items follow)
+  int nT;       // sequences in perm
+  int nB, nS;   // tail items of the big tails (perm's first ones), shared items
 };
 
 struct SItem {
@@ -175,62 +183,130 @@ __device__ __forceinline__ int part_items(const SParams& p, int R, bool shared) 
 // otherwise every sequence is its own group and PA_DEV_BAD_GROUP is set), the
 // shared blocks used per group, the partitions of every sequence (written to
 // the workspace by CTA 0 for the merge), item counts and their prefix sums.
-// Returns the number of items.
+// Tail items are ordered by size, largest first (a stable counting sort of
+// the sequences on the size of their largest tail item, in kKH buckets per
+// class), so the items handed out last are the shortest.  tmp: scratch of
+// 3 * B + 2 * kKH * NTH / 32 + 1 ints (the stage ring, unused until the
+// first load).  Returns the number of items.
 template <int NTH>
-__device__ int build_tables(const SParams& p, Tables& t, int* wsum) {
+__device__ int build_tables(const SParams& p, Tables& t, int* wsum, int* tmp) {
+  constexpr int NW = NTH / 32;
+  constexpr int NK = 2 * kKH;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Lmax = p.max_blocks * p.bs;
-  for (int b = threadIdx.x; b < p.B; b += NTH) {
-    int L = __ldg(&p.context_lens[b]);
-    if (L < 0 || L > Lmax) {
-      if (blockIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_LEN);
-      L = L < 0 ? 0 : Lmax;
+  int* key = tmp;                 // [B] bucket of each sequence (-1: no tail item)
+  int* nit = tmp + p.B;           // [B] tail items of each sequence
+  int* gid = tmp + 2 * p.B;       // [B] group of each sequence
+  int* hist = tmp + 3 * p.B;      // [NK * NW + 1] per (bucket, warp) counts, then offsets
+  for (int i = threadIdx.x; i <= NK * NW; i += NTH) hist[i] = 0;
+  // One round of global loads for the lengths and the descriptor: each
+  // thread issues all of its loads before storing any.
+  const int nld = max(p.B, p.ng + 1);
+  for (int i0 = 0; i0 < nld; i0 += kLB * NTH) {
+    int lv[kLB], gv[kLB], sv[kLB];
+#pragma unroll
+    for (int k = 0; k < kLB; ++k) {
+      const int i = i0 + k * NTH + threadIdx.x;
+      lv[k] = i < p.B ? __ldg(&p.context_lens[i]) : 0;
+      gv[k] = i <= p.ng ? __ldg(&p.group_start[i]) : 0;
+      sv[k] = i < p.ng ? __ldg(&p.shared_blocks[i]) : 0;
     }
-    t.Ls[b] = L;
+#pragma unroll
+    for (int k = 0; k < kLB; ++k) {
+      const int i = i0 + k * NTH + threadIdx.x;
+      if (i < p.B) {
+        int L = lv[k];
+        if (L < 0 || L > Lmax) {
+          if (blockIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_LEN);
+          L = L < 0 ? 0 : Lmax;
+        }
+        t.Ls[i] = L;
+      }
+      if (i <= p.ng) t.gsm[i] = gv[k];
+      if (i < p.ng) t.Sg[i] = sv[k];
+    }
   }
+  __syncthreads();
   bool ok = true;
   for (int g = threadIdx.x; g < p.ng; g += NTH) {
-    const int a = __ldg(&p.group_start[g]), c = __ldg(&p.group_start[g + 1]);
+    const int a = t.gsm[g], c = t.gsm[g + 1];
     if (a > c || a < 0 || c > p.B) ok = false;
   }
-  if (threadIdx.x == 0 && (__ldg(&p.group_start[0]) != 0 || __ldg(&p.group_start[p.ng]) != p.B)) ok = false;
+  if (threadIdx.x == 0 && (t.gsm[0] != 0 || t.gsm[p.ng] != p.B)) ok = false;
   const bool valid = __syncthreads_and(ok) != 0;
-  if (!valid && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_GROUP);
+  if (!valid) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_status_shared, PA_DEV_BAD_GROUP);
+    for (int g = threadIdx.x; g <= p.B; g += NTH) t.gsm[g] = g;
+    __syncthreads();
+  }
   t.ngE = valid ? p.ng : p.B;
-  for (int g = threadIdx.x; g <= t.ngE; g += NTH) t.gsm[g] = valid ? __ldg(&p.group_start[g]) : g;
-  __syncthreads();
   // Items are handed out in three classes, the larger first, so the last
   // ones to start are short: tail items larger than a full shared item
   // (shared_items_per_part's usual two KV heads x ps_blocks blocks), the
   // shared items, then the other tail items.
   const int ipt = part_items(p, p.G, false);
   const int big_tokens = p.ps_blocks * p.bs * 2 / 4;   // a tail item covers 4 KV heads
+  const int chunk = (p.B + NW - 1) / NW;               // sequences per warp in the placement pass
   for (int g = threadIdx.x; g < t.ngE; g += NTH) {
     const int s0 = t.gsm[g], s1 = t.gsm[g + 1];
     int S = 0;
     if (valid && s1 - s0 >= 2) {
-      S = min(max(__ldg(&p.shared_blocks[g]), 0), p.max_blocks);
-      for (int b = s0; b < s1; ++b) S = min(S, t.Ls[b] / p.bs);
+      S = min(max(t.Sg[g], 0), p.max_blocks);
+      for (int b = s0; b < s1; ++b) S = min(S, t.Ls[b] >> p.bs_shift);
     }
     t.Sg[g] = S;
     const int nspg = S > 0 ? ceil_div(S, p.ps_blocks) : 0;
-    t.shc[g] = nspg * part_items(p, (s1 - s0) * p.G, true);
-    t.preS[g] = t.shc[g];
-    for (int b = s0; b < s1; ++b) {
-      int nsp, ntp;
-      seq_parts(p, S, t.Ls[b], nsp, ntp);
-      const bool big = min(t.Ls[b] - S * p.bs, p.pt_tokens) > big_tokens;
-      t.preB[b] = big ? ntp * ipt : 0;
-      t.preM[b] = big ? 0 : ntp * ipt;
-      if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
-    }
+    t.preS[g] = nspg * part_items(p, (s1 - s0) * p.G, true);
+    for (int b = s0; b < s1; ++b) gid[b] = g;
   }
   __syncthreads();
-  block_scan<NTH>(t.preB, p.B, wsum);
-  block_scan<NTH>(t.preM, p.B, wsum);
+  for (int b = threadIdx.x; b < p.B; b += NTH) {
+    const int S = t.Sg[gid[b]];
+    int nsp, ntp;
+    seq_parts(p, S, t.Ls[b], nsp, ntp);
+    const int first = min(max(t.Ls[b] - S * p.bs, 0), p.pt_tokens);   // tokens of its largest tail item
+    const int kb = min((first + p.bs - 1) >> p.bs_shift, kKH - 1);
+    const int d = (first > big_tokens ? 0 : kKH) + (kKH - 1 - kb);
+    nit[b] = ntp * ipt;
+    key[b] = ntp > 0 ? d : -1;
+    if (ntp > 0) atomicAdd(&hist[d * NW + b / chunk], 1);
+    t.one[b] = nsp + ntp == 1;
+    if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
+  }
+  __syncthreads();
+  block_scan<NTH>(hist, NK * NW, wsum);
   block_scan<NTH>(t.preS, t.ngE, wsum);
-  t.nB = t.preB[p.B];
+  const int nT = hist[NK * NW];
+  const int nbig = hist[kKH * NW];       // sequences in the big-tail buckets
+  __syncthreads();
+  // placement: warp w walks its sequences in order, so equal buckets keep
+  // sequence order and every CTA computes the same permutation
+  const int b0 = warp * chunk, b1 = min(p.B, b0 + chunk);
+  for (int base = b0; base < b1; base += 32) {
+    const int b = base + lane;
+    const int d = b < b1 ? key[b] : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, d);
+    const int rank = __popc(m & ((1u << lane) - 1u));
+    int pos = 0;
+    if (d >= 0) pos = hist[d * NW + warp] + rank;
+    __syncwarp();
+    if (d >= 0) {
+      t.perm[pos] = b;
+      t.preT[pos] = nit[b];
+      if (rank == 0) hist[d * NW + warp] += __popc(m);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  block_scan<NTH>(t.preT, nT, wsum);
+  t.nT = nT;
+  t.nB = t.preT[nbig];
   t.nS = t.preS[t.ngE];
-  return t.nB + t.nS + t.preM[p.B];
+  // the scratch is the stage ring: order these generic writes before the
+  // TMA loads that will overwrite it
+  fence_proxy_async_smem();
+  __syncthreads();
+  return t.preT[nT] + t.nS;
 }
 
 // Largest index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x):
@@ -255,10 +331,10 @@ __device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i,
     g = last_le(t.preS, t.ngE, r);      // the group holding shared item r
     r -= t.preS[g];
   } else {
-    const int* pre = i < t.nB ? t.preB : t.preM;
-    const int k = i < t.nB ? i : i - t.nB - t.nS;
-    b = last_le(pre, p.B, k);           // the sequence holding tail item k
-    rr = k - pre[b];
+    const int k = i < t.nB ? i : i - t.nS;
+    const int j = last_le(t.preT, t.nT, k);   // the sequence holding tail item k
+    b = t.perm[j];
+    rr = k - t.preT[j];
     g = last_le(t.gsm, t.ngE, b);       // its group
     r = 0;
   }
@@ -302,8 +378,8 @@ __device__ __forceinline__ void s_item(const SParams& p, const Tables& t, int i,
     const int T0 = S * p.bs + part * p.pt_tokens;
     const int L = t.Ls[b];
     it.t1 = max(T0, min(L, T0 + p.pt_tokens));
-    it.jb = T0 / p.bs;
-    it.je = ceil_div(it.t1, p.bs);
+    it.jb = T0 >> p.bs_shift;
+    it.je = (it.t1 + p.bs - 1) >> p.bs_shift;
     int nsp, ntp;
     seq_parts(p, S, L, nsp, ntp);
     it.slot = nsp + part;
@@ -493,8 +569,9 @@ __device__ __forceinline__ void run_rows(const SParams& p, const Tables& t, cons
     const int rho = rbase + 8 * n + g;
     const bool ok = active && rho < it.R;
     const int gr = it.row0 + rho;
-    const int seq = it.s0 + (ok ? gr / p.G : 0);
-    const int qh = kvh * p.G + (ok ? gr % p.G : 0);
+    const int mem = ok ? (gr * p.ginv) >> 16 : 0;
+    const int seq = it.s0 + mem;
+    const int qh = kvh * p.G + (ok ? gr - mem * p.G : 0);
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(
         static_cast<const unsigned char*>(p.q) + ((size_t)seq * p.Hq + (ok ? qh : 0)) * (D * 2));
 #pragma unroll
@@ -603,12 +680,11 @@ __device__ __forceinline__ void run_rows(const SParams& p, const Tables& t, cons
       const int rho = rbase + 8 * n + 2 * tq + e;
       if (rho >= it.R) continue;
       const int gr = it.row0 + rho;
-      const int seq = it.s0 + gr / p.G;
-      const int qh = kvh * p.G + gr % p.G;
-      int nsp, ntp;
-      seq_parts(p, it.S, t.Ls[seq], nsp, ntp);
+      const int mem = (gr * p.ginv) >> 16;
+      const int seq = it.s0 + mem;
+      const int qh = kvh * p.G + gr - mem * p.G;
       const size_t bh = (size_t)seq * p.Hq + qh;
-      if (nsp + ntp == 1) {
+      if (t.one[seq]) {
         const float inv = lh[n][e] > 0.f ? 1.f / lh[n][e] : 0.f;
         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + bh * D;
 #pragma unroll
@@ -647,16 +723,17 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   uint64_t* qempty = qfull + kQ;                      // [kQ] item queue: index read by every consumer
   volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + kQ);
   int* qid = const_cast<int*>(abort_flag) + 4;        // [kQ]
-  int* wsum = qid + kQ;                               // [8]
+  SItem* qit = reinterpret_cast<SItem*>(qid + kQ);    // [kQ] the items behind qid
+  int* wsum = reinterpret_cast<int*>(qit + kQ);       // [8]
   const int ngMax = max(p.ng, p.B);
   Tables t;
   t.Ls = wsum + 8;
-  t.preB = t.Ls + p.B;
-  t.preM = t.preB + p.B + 1;
-  t.gsm = t.preM + p.B + 1;
+  t.perm = t.Ls + p.B;
+  t.preT = t.perm + p.B;
+  t.gsm = t.preT + p.B + 1;
   t.preS = t.gsm + ngMax + 1;
-  t.shc = t.preS + ngMax + 1;
-  t.Sg = t.shc + ngMax;
+  t.Sg = t.preS + ngMax + 1;
+  t.one = reinterpret_cast<unsigned char*>(t.Sg + ngMax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the merge kernel (a programmatic dependent on eager calls) may be
@@ -675,7 +752,10 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
     fence_mbar_init();
   }
 
-  const int n_items = build_tables<kST>(p, t, wsum);
+  // the producer's first item index is fetched while the tables are built
+  int pend = 0;
+  if (warp == kSW && lane == 0) pend = atomicAdd(p.ws_next, 1);
+  const int n_items = build_tables<kST>(p, t, wsum, reinterpret_cast<int*>(tilesK));
 
   if (warp == kSW) {
     // ------------------------------------------------------------ producer
@@ -693,15 +773,19 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
     // Items are taken from the launch-wide counter as this CTA gets to them
     // (the next index is fetched while the current item's loads go out) and
     // passed to the consumers through a queue of kQ slots.
-    int pend = 0;
-    if (lane == 0) pend = atomicAdd(p.ws_next, 1);
     for (int kq = 0;; ++kq) {
       const int q = kq % kQ;
-      int v = -1;
+      // the item is described once here and handed to the consumers with
+      // its index
+      const int v = __shfl_sync(0xffffffffu, pend < n_items ? pend : -1, 0);
+      SItem it;
+      if (v >= 0) s_item(p, t, v, it);
       if (lane == 0) {
         if (!*abort_flag && mbar_wait(&qempty[q], ((uint32_t)(kq / kQ) & 1u) ^ 1u)) {
-          v = pend < n_items ? pend : -1;
-          if (v >= 0) pend = atomicAdd(p.ws_next, 1);
+          if (v >= 0) {
+            pend = atomicAdd(p.ws_next, 1);
+            qit[q] = it;
+          }
           qid[q] = v;
           mbar_arrive(&qfull[q]);
         } else if (!*abort_flag) {
@@ -709,10 +793,7 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
           *abort_flag = 1;
         }
       }
-      v = __shfl_sync(0xffffffffu, v, 0);
-      if (v < 0) break;
-      SItem it;
-      s_item(p, t, v, it);
+      if (v < 0 || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const int32_t* row = p.block_tables + (size_t)it.s0 * p.max_blocks;
       const int nblk = it.je - it.jb;
       const int nh = 4 / it.bps;
@@ -802,11 +883,11 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
       }
     }
     const int v = live ? qid[q] : -1;
+    SItem it;
+    if (v >= 0) it = qit[q];
     __syncwarp();
     if (live && lane == 0) mbar_arrive(&qempty[q]);
     if (v < 0) break;
-    SItem it;
-    s_item(p, t, v, it);
     const int hd = warp / it.wh;
     const int rbase = (warp % it.wh) * 8 * it.nt;
     const bool active = hd < 4 / it.bps && it.kvh0 + hd < p.Hkv && rbase < it.R;
@@ -1054,17 +1135,20 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   prm.max_parts = pl.max_parts;
   prm.tile_bytes = (uint32_t)(block_size * head_dim * 2);
   prm.qscale = scale * kLog2eS;
+  prm.bs_shift = block_size == 4 ? 2 : block_size == 8 ? 3 : block_size == 16 ? 4 : 5;
+  prm.ginv = (65536 + prm.G - 1) / prm.G;
 
   // Stages of four tiles: as many as fit beside
   // the tables for two CTAs per SM (2..6), or, when a stage is so large that
   // two do not fit, one CTA per SM with up to 3.
   // shared memory: stages (K and V tiles), their two mbarriers each, the
   // item queue's 2 x kQ mbarriers, the abort flag (16 bytes), qid[kQ], then
-  // the tables: wsum[8], Ls[B], preB[B+1], preM[B+1], gsm[ngMax+1],
-  // preS[ngMax+1], shc[ngMax], Sg[ngMax]
+  // the queue's items qit[kQ], then the tables: wsum[8], Ls[B], perm[B],
+  // preT[B+1], gsm[ngMax+1], preS[ngMax+1], Sg[ngMax], one[B] (bytes)
   const size_t stage = 2 * (size_t)kTiles * prm.tile_bytes;
   const size_t ngMax = (size_t)(num_groups > num_seqs ? num_groups : num_seqs);
-  const size_t tables = 2 * kQ * sizeof(uint64_t) + 16 + 4 * (kQ + 8 + 3 * (size_t)num_seqs + 2 + 4 * ngMax + 2);
+  const size_t tables = 2 * kQ * sizeof(uint64_t) + 16 + 4 * (size_t)kQ + kQ * sizeof(SItem) +
+                        4 * (8 + 3 * (size_t)num_seqs + 1 + 3 * ngMax + 2) + ((size_t)num_seqs + 3) / 4 * 4;
   const size_t per_cta = (227 * 1024) / 2 - 1024;
   int ns = (int)((per_cta - tables - kAlign) / (stage + 16));
   if (ns >= 2) {
@@ -1074,6 +1158,8 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
     if (ns > 3) ns = 3;
     if (ns < 1) return PA_ERR_SHAPE;
   }
+  // the table build's scratch lives in the stage ring until the first load
+  if ((3 * (size_t)num_seqs + 2 * kKH * (kST / 32) + 1) * 4 > (size_t)ns * stage) return PA_ERR_SHAPE;
   prm.nstage = ns;
   const size_t smem = (size_t)ns * (stage + 2 * sizeof(uint64_t)) + tables + kAlign;
 
