@@ -172,6 +172,42 @@ __device__ void block_scan(int* arr, int n, int* wsum) {
   __syncthreads();
 }
 
+// Two block-wide exclusive scans at once (a[0..na), b[0..nb)), in place,
+// with a[na] and b[nb] the totals; wsum holds 16 ints.
+template <int NTH>
+__device__ void block_scan2(int* a, int na, int* b, int nb, int* wsum) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pa = (na + NTH - 1) / NTH, pb = (nb + NTH - 1) / NTH;
+  const int a0 = min(na, (int)threadIdx.x * pa), a1 = min(na, a0 + pa);
+  const int b0 = min(nb, (int)threadIdx.x * pb), b1 = min(nb, b0 + pb);
+  int sa = 0, sb = 0;
+  for (int i = a0; i < a1; ++i) sa += a[i];
+  for (int i = b0; i < b1; ++i) sb += b[i];
+  int ia = sa, ib = sb;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, ia, off);
+    const int yb = __shfl_up_sync(0xffffffffu, ib, off);
+    if (lane >= off) ia += ya, ib += yb;
+  }
+  if (lane == 31) wsum[warp] = ia, wsum[8 + warp] = ib;
+  __syncthreads();
+  int ra = ia - sa, rb = ib - sb;
+  for (int w = 0; w < warp; ++w) ra += wsum[w], rb += wsum[8 + w];
+  for (int i = a0; i < a1; ++i) {
+    const int c = a[i];
+    a[i] = ra;
+    ra += c;
+  }
+  for (int i = b0; i < b1; ++i) {
+    const int c = b[i];
+    b[i] = rb;
+    rb += c;
+  }
+  if (threadIdx.x == NTH - 1) a[na] = ra, b[nb] = rb;
+  __syncthreads();
+}
+
 // Items of one shared partition of a group with R rows per KV head, and of
 // one tail partition (KV heads grouped as the stages hold them).
 __device__ __forceinline__ int part_items(const SParams& p, int R, bool shared) {
@@ -260,28 +296,35 @@ __device__ int build_tables(const SParams& p, Tables& t, int* wsum, int* tmp) {
     for (int b = s0; b < s1; ++b) gid[b] = g;
   }
   __syncthreads();
-  for (int b = threadIdx.x; b < p.B; b += NTH) {
-    const int S = t.Sg[gid[b]];
-    int nsp, ntp;
-    seq_parts(p, S, t.Ls[b], nsp, ntp);
-    const int first = min(max(t.Ls[b] - S * p.bs, 0), p.pt_tokens);   // tokens of its largest tail item
-    const int kb = min((first + p.bs - 1) >> p.bs_shift, kKH - 1);
-    const int d = (first > big_tokens ? 0 : kKH) + (kKH - 1 - kb);
-    nit[b] = ntp * ipt;
-    key[b] = ntp > 0 ? d : -1;
-    if (ntp > 0) atomicAdd(&hist[d * NW + b / chunk], 1);
-    t.one[b] = nsp + ntp == 1;
-    if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
+  // per-sequence pass by the warp that places the sequence later: its
+  // (bucket, warp) counts need no atomics
+  const int b0 = warp * chunk, b1 = min(p.B, b0 + chunk);
+  for (int base = b0; base < b1; base += 32) {
+    const int b = base + lane;
+    int d = -1;
+    if (b < b1) {
+      const int S = t.Sg[gid[b]];
+      int nsp, ntp;
+      seq_parts(p, S, t.Ls[b], nsp, ntp);
+      const int first = min(max(t.Ls[b] - S * p.bs, 0), p.pt_tokens);   // tokens of its largest tail item
+      const int kb = min((first + p.bs - 1) >> p.bs_shift, kKH - 1);
+      d = ntp > 0 ? (first > big_tokens ? 0 : kKH) + (kKH - 1 - kb) : -1;
+      nit[b] = ntp * ipt;
+      key[b] = d;
+      t.one[b] = nsp + ntp == 1;
+      if (blockIdx.x == 0) p.ws_parts[b] = nsp + ntp;
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, d);
+    if (d >= 0 && (m & ((1u << lane) - 1u)) == 0) hist[d * NW + warp] += __popc(m);
+    __syncwarp();
   }
   __syncthreads();
-  block_scan<NTH>(hist, NK * NW, wsum);
-  block_scan<NTH>(t.preS, t.ngE, wsum);
+  block_scan2<NTH>(hist, NK * NW, t.preS, t.ngE, wsum);
   const int nT = hist[NK * NW];
   const int nbig = hist[kKH * NW];       // sequences in the big-tail buckets
   __syncthreads();
   // placement: warp w walks its sequences in order, so equal buckets keep
   // sequence order and every CTA computes the same permutation
-  const int b0 = warp * chunk, b1 = min(p.B, b0 + chunk);
   for (int base = b0; base < b1; base += 32) {
     const int b = base + lane;
     const int d = b < b1 ? key[b] : -1;
@@ -724,10 +767,10 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + kQ);
   int* qid = const_cast<int*>(abort_flag) + 4;        // [kQ]
   SItem* qit = reinterpret_cast<SItem*>(qid + kQ);    // [kQ] the items behind qid
-  int* wsum = reinterpret_cast<int*>(qit + kQ);       // [8]
+  int* wsum = reinterpret_cast<int*>(qit + kQ);       // [16]
   const int ngMax = max(p.ng, p.B);
   Tables t;
-  t.Ls = wsum + 8;
+  t.Ls = wsum + 16;
   t.perm = t.Ls + p.B;
   t.preT = t.perm + p.B;
   t.gsm = t.preT + p.B + 1;
@@ -898,68 +941,107 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
   }
 }
 
-// One warp per (sequence, query head) whose sequence has several partitions:
-// out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i with M = max_i m_i.
-// Lane i < 32 computes part i's weight; each part's row of o is read as one
-// 16-byte (head_dim 128) or 8-byte vector per lane.
+// The merge: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i over a
+// (sequence, query head) row's partials in slot order, M = max_i m_i.  One
+// warp takes kMR rows; every load those rows need for their first kMP
+// partials (the sequence's partition count, the (m, l) pairs, the rows of o)
+// is issued before any is used, so the warp waits for one round trip to L2;
+// partials past kMP (long private tails) follow in a loop.  Lane l holds dims
+// l*D/32 .. l*D/32 + D/32 - 1.
+constexpr int kMR = 4;
+constexpr int kMP = 2;
+
+template <int VPL>
+__device__ __forceinline__ void ld_cg(const float* src, float (&v)[VPL]) {
+  if constexpr (VPL == 4) {
+    const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else {
+    const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+    v[0] = t.x, v[1] = t.y;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
-  constexpr int VPL = D / 32;      // dims per lane
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int VPL = D / 32;
+  const long long nrows = (long long)p.B * p.Hq;
+  const long long r0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kMR;
   const int lane = threadIdx.x & 31;
-  if (gw >= (long long)p.B * p.Hq) return;
+  if (r0 >= nrows) return;
   // a programmatic dependent of the decode kernel on eager calls: the
   // partition counts and partials are read once that grid has completed
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = (int)(gw / p.Hq);
-  const int nparts = p.ws_parts[b];
-  if (nparts <= 1) return;
-  const size_t base = (size_t)gw * p.max_parts;
-  float M = -INFINITY;
-  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[(base + i) * 2]);
+  const int sp = min(kMP, p.max_parts);
+  int np[kMR];
+  float2 ml[kMR];          // lane i < sp: partial i's (m, l)
+  float ov[kMR][kMP][VPL];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float den = 0.f;
-  float acc[VPL];
+  for (int r = 0; r < kMR; ++r) {
+    const bool ok = r0 + r < nrows;
+    const long long row = ok ? r0 + r : r0;
+    const size_t base = (size_t)row * p.max_parts;
+    np[r] = ok ? __ldcg(&p.ws_parts[row / p.Hq]) : 0;
+    ml[r] = lane < sp ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base + lane) : make_float2(-INFINITY, 0.f);
 #pragma unroll
-  for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
-  for (int i0 = 0; i0 < nparts; i0 += 32) {
-    const int i = i0 + lane;
-    float w = 0.f;
-    if (i < nparts) {
-      const float mi = p.ws_ml[(base + i) * 2];
-      w = mi == -INFINITY ? 0.f : exp2f(mi - M);
-      den = fmaf(w, p.ws_ml[(base + i) * 2 + 1], den);
-    }
-    const int cnt = min(32, nparts - i0);
-    const float* o = p.ws_o + (base + i0) * D + lane * VPL;
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      if constexpr (VPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(o + (size_t)k * D);
-        acc[0] = fmaf(wk, v.x, acc[0]);
-        acc[1] = fmaf(wk, v.y, acc[1]);
-        acc[2] = fmaf(wk, v.z, acc[2]);
-        acc[3] = fmaf(wk, v.w, acc[3]);
+    for (int i = 0; i < kMP; ++i) {
+      if (i < sp) {
+        ld_cg<VPL>(p.ws_o + (base + i) * D + lane * VPL, ov[r][i]);
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(o + (size_t)k * D);
-        acc[0] = fmaf(wk, v.x, acc[0]);
-        acc[1] = fmaf(wk, v.y, acc[1]);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) ov[r][i][k] = 0.f;
       }
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)gw * D + lane * VPL;
-  if constexpr (VPL == 4) {
-    uint2 v;
-    v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(out) = v;
-  } else {
-    *reinterpret_cast<uint32_t*>(out) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  for (int r = 0; r < kMR; ++r) {
+    const int n = np[r];
+    if (n <= 1) continue;
+    const size_t base = (size_t)(r0 + r) * p.max_parts;
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMP; ++i) {
+      const float mi = __shfl_sync(0xffffffffu, ml[r].x, i);
+      if (i < n) M = fmaxf(M, mi);
+    }
+    if (n > kMP) {
+      for (int i = kMP + lane; i < n; i += 32) M = fmaxf(M, __ldcg(&p.ws_ml[(base + i) * 2]));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    }
+    float den = 0.f, acc[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMP; ++i) {
+      const float mi = __shfl_sync(0xffffffffu, ml[r].x, i);
+      const float li = __shfl_sync(0xffffffffu, ml[r].y, i);
+      if (i < n) {
+        const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
+        den = fmaf(w, li, den);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) acc[k] = fmaf(w, ov[r][i][k], acc[k]);
+      }
+    }
+    for (int i = kMP; i < n; ++i) {
+      const float2 mli = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base + i);
+      float v[VPL];
+      ld_cg<VPL>(p.ws_o + (base + i) * D + lane * VPL, v);
+      const float w = mli.x == -INFINITY ? 0.f : exp2f(mli.x - M);
+      den = fmaf(w, mli.y, den);
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) acc[k] = fmaf(w, v[k], acc[k]);
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(r0 + r) * D + lane * VPL;
+    if constexpr (VPL == 4) {
+      uint2 v;
+      v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(out) = v;
+    } else {
+      *reinterpret_cast<uint32_t*>(out) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
   }
 }
 
@@ -1000,11 +1082,12 @@ int shared_occupancy(const void* kernel, size_t smem, int dev) {
   return occ;
 }
 
-// Automatic shared partition: 512 tokens (at least one block).  With work
-// items handed out at run time, longer shared items balance as well as short
-// ones and cost fewer items and partials: c5 0.133 ms per call at 256 tokens,
-// 0.125 at 512, 0.132 at 1024.
-constexpr int kSharedPartTokens = 512;
+// Automatic shared partition: 1024 tokens (at least one block).  With work
+// items handed out at run time, largest tails first, long shared items
+// balance against the tails and cost fewer items and partials: c5 (1024-token
+// prompts) 0.1140 ms per call at 512 tokens, 0.1174 at 768, 0.1086 at 1024,
+// 0.1080 at 1536 and 2048 (one box).
+constexpr int kSharedPartTokens = 1024;
 
 struct SharedPlan {
   int ps_blocks, pt_tokens, max_parts;
@@ -1100,6 +1183,7 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   const size_t need = pa_decode_shared_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
                                                        max_blocks_per_seq, block_size, partition_size, num_groups);
   if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
 
   int dev = 0;
   if (!ck(cudaGetDevice(&dev), "cudaGetDevice")) return PA_ERR_CUDA;
@@ -1143,12 +1227,12 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   // two do not fit, one CTA per SM with up to 3.
   // shared memory: stages (K and V tiles), their two mbarriers each, the
   // item queue's 2 x kQ mbarriers, the abort flag (16 bytes), qid[kQ], then
-  // the queue's items qit[kQ], then the tables: wsum[8], Ls[B], perm[B],
+  // the queue's items qit[kQ], then the tables: wsum[16], Ls[B], perm[B],
   // preT[B+1], gsm[ngMax+1], preS[ngMax+1], Sg[ngMax], one[B] (bytes)
   const size_t stage = 2 * (size_t)kTiles * prm.tile_bytes;
   const size_t ngMax = (size_t)(num_groups > num_seqs ? num_groups : num_seqs);
   const size_t tables = 2 * kQ * sizeof(uint64_t) + 16 + 4 * (size_t)kQ + kQ * sizeof(SItem) +
-                        4 * (8 + 3 * (size_t)num_seqs + 1 + 3 * ngMax + 2) + ((size_t)num_seqs + 3) / 4 * 4;
+                        4 * (16 + 3 * (size_t)num_seqs + 1 + 3 * ngMax + 2) + ((size_t)num_seqs + 3) / 4 * 4;
   const size_t per_cta = (227 * 1024) / 2 - 1024;
   int ns = (int)((per_cta - tables - kAlign) / (stage + 16));
   if (ns >= 2) {
@@ -1176,7 +1260,7 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   if (!ck(cudaLaunchKernel(kern, dim3(grid), dim3(kST), args, smem, (cudaStream_t)stream),
           "cudaLaunchKernel(shared_decode_kernel)"))
     return PA_ERR_CUDA;
-  const long long warps = (long long)num_seqs * num_heads;
+  const long long warps = ((long long)num_seqs * num_heads + kMR - 1) / kMR;
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
   void* margs[] = {&prm};
   if (!ck(launch_after(merge, dim3(blocks), dim3(256), margs, (cudaStream_t)stream),

@@ -50,10 +50,10 @@ def test_workspace_and_partition_arithmetic(pa):
     assert pa.partition_size(512, 32, 8, 128, 81, 16, 0) == 1296               # 1024 items: no split
     assert pa.partition_size(64, 32, 32, 128, 128, 16, 64, fp8=True) == 64
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 0, fp8=True) == 12
-    # shared-prefix decode: per (sequence, head) slots for ceil(max_ctx / 512) + 1
-    # partitions (512-token shared partitions), a partition count per sequence,
+    # shared-prefix decode: per (sequence, head) slots for ceil(max_ctx / 1024) + 1
+    # partitions (1024-token shared partitions), a partition count per sequence,
     # never less than pa_decode's
-    rows = 512 * 32 * (-(-1280 // 512) + 1)
+    rows = 512 * 32 * (-(-1280 // 1024) + 1)
     # partition counts (B ints) and the item counter, rounded to 256 bytes: (512 + 1) * 4 -> 2304
     assert pa.shared_workspace_bytes(512, 32, 8, 128, 80, 16, 0, 64) == 2304 + rows * 8 + rows * 128 * 4
     assert pa.shared_workspace_bytes(64, 32, 32, 128, 128, 16, 0, 8) >= pa.workspace_bytes(64, 32, 32, 128, 128, 16)
