@@ -178,12 +178,13 @@ int pa_decode(void* out, const void* query,
  *                  through its own row.  The two attention states are
  *                  merged by log-sum-exp (exact up to rounding: the online
  *                  softmax is associative).
- *   partition_size 0: automatic (512-token partitions of the shared blocks;
+ *   partition_size 0: automatic (1024-token partitions of the shared blocks;
  *                  the private tails as pa_decode's automatic choice);
  *                  > 0: a multiple of block_size used for both; < 0: no
  *                  split of either.
  *   workspace      at least pa_decode_shared_workspace_bytes() with the same
- *                  sizes; contents on entry do not matter
+ *                  sizes, 16-byte aligned (PA_ERR_ALIGN otherwise); contents
+ *                  on entry do not matter
  *   other arguments as for pa_decode
  *
  * Device-detected conditions (PA_DEV_BAD_GROUP): a descriptor that is not
@@ -197,7 +198,7 @@ int pa_decode(void* out, const void* query,
  * (same result, no sharing exploited).  On the stream: a 4-byte memset of
  * the work-item counter the call keeps in the workspace, the decode kernel
  * (its CTAs take work items from that counter as they free up, larger ones
- * first) and a merge kernel.
+ * first; private tails largest first) and a merge kernel.
  */
 int pa_decode_shared(void* out, const void* query,
                      const void* k_cache, const void* v_cache,

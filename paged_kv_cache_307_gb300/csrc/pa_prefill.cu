@@ -32,7 +32,11 @@
 //    mask (diagonal tile only) and scale (base 2), keeps a running max and
 //    sum, and writes P = exp2(s - m) (fp32 exponentials) back as packed
 //    bf16 over the first 32 columns of the same S buffer (tcgen05.st); at the
-//    end it reads O back, divides by the sum and stores bf16 rows.
+//    end it reads O back and divides by the sum.  A full tile's bf16 rows are
+//    staged in the Q buffer (free once the last S product has completed) and
+//    written by two TMA tile stores; a ragged tile's rows past the
+//    sequence's queries belong to the next sequence, so each thread stores
+//    its own row there.
 //  * 98 KB of shared memory and 224 threads per CTA: two CTAs per SM, so one
 //    CTA's softmax overlaps the other's MMAs.
 //  * The running max used as the exponent reference only moves when a new
@@ -127,7 +131,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-               const __grid_constant__ CUtensorMap mapV, const PrefillParams p) {
+               const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
+               const PrefillParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -464,16 +469,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
       tc_fence_after();
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    unsigned char* orow = static_cast<unsigned char*>(p.out) +
-                          (((size_t)qrow0 + q0 + qi) * p.Hq + (size_t)kvh * p.G + hh) * (kD * 2);
+    if (nt > 0 && q0 + p.QP <= nq) {
+      // A full tile: O / l as bf16 rows staged in the Q buffer (its last
+      // reader, S_{nt-1}, completed before P_{nt-1} V_{nt-1}) in the
+      // 128-byte-swizzled layout of the tile's TMA box, then two TMA stores.
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      if (have) {
-        tmem_ld32(tO + lane_off + c * 32, v);
-        tmem_ld_wait();
-      }
-      if (row_out) {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (have) {
+          tmem_ld32(tO + lane_off + c * 32, v);
+          tmem_ld_wait();
+        }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t w[4];
@@ -484,7 +490,42 @@ prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
             const __nv_bfloat162 pk = __floats2bfloat162_rn(a0, a1);
             w[e] = *reinterpret_cast<const uint32_t*>(&pk);
           }
-          st_v4(orow + (c * 32 + g * 8) * 2, make_uint4(w[0], w[1], w[2], w[3]));
+          const int ch = c * 4 + g;                 // 16-byte chunk of the row, 0..15
+          *reinterpret_cast<uint4*>(smem + kOffQ + (ch >> 3) * kQHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_sync(1, 128);
+      if (warp == 2 && lane == 0) {
+        tma_store_4d(&mapO, smem + kOffQ, 0, kvh * p.G, qrow0 + q0, 0);
+        tma_store_4d(&mapO, smem + kOffQ + kQHalf, 64, kvh * p.G, qrow0 + q0, 0);
+        bulk_commit();
+        bulk_wait_all();
+      }
+    } else {
+      unsigned char* orow = static_cast<unsigned char*>(p.out) +
+                            (((size_t)qrow0 + q0 + qi) * p.Hq + (size_t)kvh * p.G + hh) * (kD * 2);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (have) {
+          tmem_ld32(tO + lane_off + c * 32, v);
+          tmem_ld_wait();
+        }
+        if (row_out) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a0 = have ? __uint_as_float(v[g * 8 + 2 * e]) * inv : 0.f;
+              const float a1 = have ? __uint_as_float(v[g * 8 + 2 * e + 1]) * inv : 0.f;
+              const __nv_bfloat162 pk = __floats2bfloat162_rn(a0, a1);
+              w[e] = *reinterpret_cast<const uint32_t*>(&pk);
+            }
+            st_v4(orow + (c * 32 + g * 8) * 2, make_uint4(w[0], w[1], w[2], w[3]));
+          }
         }
       }
     }
@@ -530,7 +571,7 @@ static int prefill_impl(void* out, const void* query, const int32_t* query_start
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
 
   const int QP = 128 / G;
-  CUtensorMap mapQ, mapK, mapV;
+  CUtensorMap mapQ, mapK, mapV, mapO;
   {
     // queries as [rows, Hq, D] (one more unit dimension for the 4-D copy)
     const uint64_t dims[4] = {128, (uint64_t)num_heads, (uint64_t)rows, 1};
@@ -538,6 +579,11 @@ static int prefill_impl(void* out, const void* query, const int32_t* query_start
     const uint32_t box[4] = {64, (uint32_t)G, (uint32_t)QP, 1};
     if (!encode_map(&mapQ, query, PA_BF16, 4, dims, str, box, true)) {
       note_host_error("cuTensorMapEncodeTiled failed for the query tile");
+      return PA_ERR_CUDA;
+    }
+    // the output as the same [rows, Hq, D] view, written one full tile per store
+    if (!encode_map(&mapO, out, PA_BF16, 4, dims, str, box, true)) {
+      note_host_error("cuTensorMapEncodeTiled failed for the output tile");
       return PA_ERR_CUDA;
     }
   }
@@ -577,7 +623,7 @@ static int prefill_impl(void* out, const void* query, const int32_t* query_start
                                       : (long long)prm.n_qt * num_seqs;
   const long long grid = tiles * num_kv_heads;
   const size_t smem = kSmemBytes + (query_start ? 4 * ((size_t)num_seqs + 1 + 8) : 0);
-  void* args[] = {&mapQ, &mapK, &mapV, &prm};
+  void* args[] = {&mapQ, &mapK, &mapV, &mapO, &prm};
   if (!ck(cudaLaunchKernel(reinterpret_cast<const void*>(&prefill_kernel), dim3((unsigned)grid), dim3(kThreads),
                            args, smem, (cudaStream_t)stream),
           "cudaLaunchKernel(prefill_kernel)"))
