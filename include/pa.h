@@ -178,8 +178,12 @@ int pa_decode(void* out, const void* query,
  *                  through its own row.  The two attention states are
  *                  merged by log-sum-exp (exact up to rounding: the online
  *                  softmax is associative).
- *   partition_size 0: automatic (1024-token partitions of the shared blocks;
- *                  the private tails as pa_decode's automatic choice);
+ *   partition_size 0: automatic: partitions of the shared blocks of 1024,
+ *                  512, 256 or 128 tokens, the largest that gives at least
+ *                  152 shared items if every group shared its whole longest
+ *                  context (host arithmetic on num_seqs, num_groups,
+ *                  num_kv_heads and max_blocks_per_seq); the private tails
+ *                  as pa_decode's automatic choice;
  *                  > 0: a multiple of block_size used for both; < 0: no
  *                  split of either.
  *   workspace      at least pa_decode_shared_workspace_bytes() with the same

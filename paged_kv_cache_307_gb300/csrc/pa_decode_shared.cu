@@ -1082,12 +1082,17 @@ int shared_occupancy(const void* kernel, size_t smem, int dev) {
   return occ;
 }
 
-// Automatic shared partition: 1024 tokens (at least one block).  With work
-// items handed out at run time, largest tails first, long shared items
-// balance against the tails and cost fewer items and partials: c5 (1024-token
-// prompts) 0.1140 ms per call at 512 tokens, 0.1174 at 768, 0.1086 at 1024,
-// 0.1080 at 1536 and 2048 (one box).
-constexpr int kSharedPartTokens = 1024;
+// Automatic shared partition: the largest of 1024, 512, 256 and 128 tokens
+// whose shared items, counted as if every group shared its whole longest
+// context, number at least half of a grid of two CTAs on each of 152 SMs
+// (host arithmetic only, like pa_decode's partition rule).  With tail items
+// handed out largest first, long shared items balance against the tails
+// and cost fewer items and partials, until a single shared item is a large
+// share of a CTA's work.  c5-shaped batches (1024-token prompts, 8 samples,
+// ms per call): 64 prompts 0.1073 at 1024 tokens, 0.1168 at 512; 32 prompts
+// 0.0841 at 1024, 0.0718 at 512; 16 prompts 0.0709 at 1024, 0.0552 at 512,
+// 0.0564 at 256; 8 prompts 0.0473 at 512, 0.0398 at 256, 0.0456 at 128.
+constexpr int kSharedRefCtas = 2 * 152;
 
 struct SharedPlan {
   int ps_blocks, pt_tokens, max_parts;
@@ -1102,7 +1107,7 @@ bool shared_eligible(int num_seqs, int num_heads, int num_kv_heads, int head_dim
 }
 
 SharedPlan shared_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int max_blocks, int block_size,
-                       int partition_size) {
+                       int partition_size, int num_groups) {
   SharedPlan pl;
   const int max_ctx = max_blocks * block_size;
   const int G = num_heads / num_kv_heads;
@@ -1113,9 +1118,17 @@ SharedPlan shared_plan(int num_seqs, int num_heads, int num_kv_heads, int head_d
     pl.ps_blocks = partition_size / block_size;
     pl.pt_tokens = partition_size;
   } else {
-    pl.ps_blocks = kSharedPartTokens / block_size > 0 ? kSharedPartTokens / block_size : 1;
+    const int ng = num_groups > 0 ? num_groups : 1;
+    const int R = (num_seqs + ng - 1) / ng * G;                     // rows of an average group
+    const int ipp = R <= 16 ? (num_kv_heads + 3) / 4 : (R + 31) / 32 * ((num_kv_heads + 1) / 2);
+    int pst = 128;
+    for (int cand = 1024; cand >= 128; cand >>= 1)
+      if ((long long)ng * ipp * (max_ctx / cand) >= kSharedRefCtas / 2) {
+        pst = cand;
+        break;
+      }
+    pl.ps_blocks = pst / block_size > 0 ? pst / block_size : 1;
     pl.pt_tokens = pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks, block_size, 0);
-    (void)G;
   }
   if (pl.pt_tokens > max_ctx) pl.pt_tokens = max_ctx;
   if (pl.ps_blocks > max_blocks) pl.ps_blocks = max_blocks;
@@ -1153,7 +1166,8 @@ extern "C" size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, 
     return plain;
   if (!shared_eligible(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_groups, PA_BF16)) return plain;
   const SharedPlan pl =
-      shared_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size);
+      shared_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size,
+                  num_groups);
   const size_t need = pl.parts_bytes + pl.ml_bytes + pl.o_bytes;
   return need > plain ? need : plain;
 }
@@ -1179,7 +1193,8 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
   if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
   const SharedPlan pl =
-      shared_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size);
+      shared_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size,
+                  num_groups);
   const size_t need = pa_decode_shared_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
                                                        max_blocks_per_seq, block_size, partition_size, num_groups);
   if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
