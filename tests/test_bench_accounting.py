@@ -93,3 +93,42 @@ def test_mixed_round_packing():
     # every query's context fits its table row
     bs = m["block_size"]
     assert (-(-lens // bs) <= m["block_tables"].shape[1]).all()
+
+
+def _sampler_with(lines, t0, t1):
+    import bench
+    s = bench.ClockSampler(0)
+    s.proc = type("P", (), {"terminate": lambda self: None, "wait": lambda self, timeout=None: 0,
+                            "kill": lambda self: None})()
+    s.t = type("T", (), {"join": lambda self, timeout=None: None})()
+    s.lines = list(lines)
+    s.t0, s.t1 = t0, t1
+    return s.stop()
+
+
+def _smi(ts, mhz, reasons=("Not Active",) * 4):
+    import datetime
+    stamp = datetime.datetime.fromtimestamp(ts).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([stamp, "0", str(mhz), "2070", "900.0", "0x0"] + list(reasons))
+
+
+def test_clock_record_keeps_the_timed_region():
+    # 20 ms samples from 1000.00 s: an idle lead-in at 1000 MHz, the timed
+    # region at 2070 MHz from 1000.30 to 1000.50 s, a tail at 1500 MHz
+    t = [1000.0 + 0.02 * i for i in range(40)]
+    mhz = [1000 if x < 1000.3 else 2070 if x <= 1000.5 else 1500 for x in t]
+    r = _sampler_with([_smi(x, m) for x, m in zip(t, mhz)], 1000.3, 1000.5)
+    assert r["sm_mhz"] == 2070 and r["which"] == "inside the timed region"
+    assert r["samples"] == 11 and r["reasons"] == [] and r["region_ms"] == pytest.approx(200.0)
+    # a throttle reason inside the region is reported, one outside it is not
+    lines = [_smi(x, m, ("Active",) + ("Not Active",) * 3 if x < 1000.1 else ("Not Active",) * 3 + ("Active",)
+                  if 1000.35 < x < 1000.45 else ("Not Active",) * 4) for x, m in zip(t, mhz)]
+    assert _sampler_with(lines, 1000.3, 1000.5)["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_record_of_a_region_shorter_than_the_sampling_interval():
+    t = [1000.0 + 0.02 * i for i in range(10)]
+    mhz = [1800, 1800, 1800, 2070, 2070, 1900, 1900, 1900, 1900, 1900]
+    # a 4 ms region between the samples at 1000.06 and 1000.08
+    r = _sampler_with([_smi(x, m) for x, m in zip(t, mhz)], 1000.0705, 1000.0745)
+    assert r["which"].startswith("nearest") and r["samples"] == 2 and r["sm_mhz"] == 2070
