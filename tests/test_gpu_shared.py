@@ -107,6 +107,29 @@ def test_shared_full_size_c5_sampled(pa):
     assert d.max() <= 2e-2 and d.mean() <= 1e-3
 
 
+# The automatic shared partition depends on the batch (1024-token partitions
+# for 64 prompts, 512 for 32, 256 for 16 and 8): each choice against the
+# oracle on sampled sequences and against plain decode on all of them.
+@pytest.mark.parametrize("batch", [64, 128, 256])
+def test_shared_automatic_partition_by_batch(pa, batch):
+    c = _case(small=False, B=batch)
+    lens = c.context_lens.cpu().numpy()
+    S = c.extra["samples"]
+    rng = np.random.default_rng(batch)
+    seqs = sorted(set(list(range(S)) + [int(np.argmax(lens)), int(np.argmin(lens))] +
+                      rng.choice(len(lens), 4, replace=False).tolist()))
+    ref = oracle_decode(c, seqs)
+    out = _run(pa, c)
+    assert pa.last_error() == 0
+    got = f64(out)
+    assert_close(got[seqs], ref, "bf16")
+    plain = torch.empty_like(c.q)
+    pa.decode(plain, c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    torch.cuda.synchronize()
+    d = np.abs(got - f64(plain))
+    assert d.max() <= 2e-2 and d.mean() <= 1e-3
+
+
 def test_invalid_descriptor_is_flagged_and_ignored(pa):
     c = _case()
     ref = oracle_decode(c)
