@@ -199,10 +199,12 @@ int pa_decode(void* out, const void* query,
  * num_heads / num_kv_heads <= 8, num_seqs <= 1024 and 1 <= num_groups <=
  * 1024 run the shared path (tensor cores, m16n8k16 bf16 products with fp32
  * accumulation, P rounded to bf16); other arguments run pa_decode unchanged
- * (same result, no sharing exploited).  On the stream: a 4-byte memset of
- * the work-item counter the call keeps in the workspace, the decode kernel
- * (its CTAs take work items from that counter as they free up, larger ones
- * first; private tails largest first) and a merge kernel.
+ * (same result, no sharing exploited).  On the stream: a one-thread kernel
+ * that clears the work-item counter the call keeps in the workspace, the
+ * decode kernel (its CTAs take work items from that counter as they free
+ * up, larger ones first; private tails largest first) and a merge kernel;
+ * on eager calls the last two are launched as programmatic dependents of
+ * the kernel before them and wait for it on the device.
  */
 int pa_decode_shared(void* out, const void* query,
                      const void* k_cache, const void* v_cache,

@@ -28,8 +28,11 @@
 //    items of each class go largest first (a stable counting sort of the
 //    sequences on their tail length), so the last items to start are the
 //    shortest and the CTAs finish close together.  A persistent
-//    grid takes items at run time from a counter in the workspace (the host
-//    clears it before each launch): the producer fetches the next index while
+//    grid takes items at run time from a counter in the workspace (cleared
+//    by a one-thread kernel launched just before, whose programmatic
+//    dependent the decode kernel is on eager calls: its CTAs build their
+//    tables while the clear runs and wait for it on the device before the
+//    first fetch): the producer fetches the next index while
 //    the current item's loads go out and passes each index to the consumer
 //    warps through a four-slot queue in shared memory, so a CTA that
 //    finishes early takes the next item instead of idling.
@@ -86,7 +89,7 @@ struct SParams {
   float* ws_ml;                 // [B*Hq*max_parts][2]  (m in log2 units, l)
   float* ws_o;                  // [B*Hq*max_parts][D]
   int32_t* ws_parts;            // [B] partitions of each sequence (shared + tail)
-  int32_t* ws_next;             // item counter, zero at launch (the host clears it)
+  int32_t* ws_next;             // item counter, zero at launch (cleared by shared_reset_kernel)
   int B, Hq, Hkv, G, ng;
   int max_blocks, bs, num_blocks;
   int ps_blocks;                // shared partition, blocks
@@ -795,10 +798,12 @@ shared_decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_cons
     fence_mbar_init();
   }
 
-  // the producer's first item index is fetched while the tables are built
+  const int n_items = build_tables<kST>(p, t, wsum, reinterpret_cast<int*>(tilesK));
+  // the item counter is cleared by the kernel launched just before this one
+  // (this grid may start early on eager calls): wait for it before fetching
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int pend = 0;
   if (warp == kSW && lane == 0) pend = atomicAdd(p.ws_next, 1);
-  const int n_items = build_tables<kST>(p, t, wsum, reinterpret_cast<int*>(tilesK));
 
   if (warp == kSW) {
     // ------------------------------------------------------------ producer
@@ -1045,7 +1050,38 @@ __global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
   }
 }
 
+// Clears the launch's item counter.  The decode kernel is its programmatic
+// dependent on eager calls: its CTAs become resident and build their tables
+// while this runs, and wait for it on the device before their first fetch.
+__global__ void __launch_bounds__(32) shared_reset_kernel(int32_t* next) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) *next = 0;
+}
+
 // ------------------------------------------------------------------ host side
+
+// A launch that may begin before the previous kernel on the stream has
+// completed (programmatic stream serialisation), on eager calls only; under
+// stream capture, or where the attribute is refused, a plain launch.
+cudaError_t launch_dependent(const void* kernel, dim3 grid, dim3 block, void** args, size_t smem,
+                             cudaStream_t stream) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();
+  }
+  return cudaLaunchKernel(kernel, grid, block, args, smem, stream);
+}
 
 std::mutex g_smu;
 std::map<std::tuple<const void*, int, int, int, int, int>, CUtensorMap> g_smaps;   // (base, nb, bs, h, d, dev)
@@ -1269,10 +1305,13 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
   const int occ = shared_occupancy(kern, smem, dev);
   if (occ <= 0) return PA_ERR_CUDA;
   const unsigned grid = (unsigned)(occ * device_sm_count());
-  if (!ck(cudaMemsetAsync(prm.ws_next, 0, sizeof(int32_t), (cudaStream_t)stream), "cudaMemsetAsync(item counter)"))
+  void* rargs[] = {&prm.ws_next};
+  if (!ck(cudaLaunchKernel(reinterpret_cast<const void*>(&shared_reset_kernel), dim3(1), dim3(32), rargs, 0,
+                           (cudaStream_t)stream),
+          "cudaLaunchKernel(shared_reset_kernel)"))
     return PA_ERR_CUDA;
   void* args[] = {&mapK, &mapV, &prm};
-  if (!ck(cudaLaunchKernel(kern, dim3(grid), dim3(kST), args, smem, (cudaStream_t)stream),
+  if (!ck(launch_dependent(kern, dim3(grid), dim3(kST), args, smem, (cudaStream_t)stream),
           "cudaLaunchKernel(shared_decode_kernel)"))
     return PA_ERR_CUDA;
   const long long warps = ((long long)num_seqs * num_heads + kMR - 1) / kMR;
