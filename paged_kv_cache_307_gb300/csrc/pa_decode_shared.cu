@@ -967,8 +967,13 @@ __device__ __forceinline__ void ld_cg(const float* src, float (&v)[VPL]) {
   }
 }
 
+// 128-thread blocks: one fits beside the decode kernel's two CTAs on an SM
+// (registers), so on eager calls some are resident before the decode grid
+// completes.
+constexpr int kMergeThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(256) shared_merge_kernel(const SParams p) {
+__global__ void __launch_bounds__(kMergeThreads) shared_merge_kernel(const SParams p) {
   constexpr int VPL = D / 32;
   const long long nrows = (long long)p.B * p.Hq;
   const long long r0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kMR;
@@ -1315,9 +1320,9 @@ extern "C" int pa_decode_shared(void* out, const void* query, const void* k_cach
           "cudaLaunchKernel(shared_decode_kernel)"))
     return PA_ERR_CUDA;
   const long long warps = ((long long)num_seqs * num_heads + kMR - 1) / kMR;
-  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  const unsigned blocks = (unsigned)((warps * 32 + kMergeThreads - 1) / kMergeThreads);
   void* margs[] = {&prm};
-  if (!ck(launch_after(merge, dim3(blocks), dim3(256), margs, (cudaStream_t)stream),
+  if (!ck(launch_after(merge, dim3(blocks), dim3(kMergeThreads), margs, (cudaStream_t)stream),
           "cudaLaunchKernel(shared_merge_kernel)"))
     return PA_ERR_CUDA;
   return PA_OK;
