@@ -183,6 +183,38 @@ int resolve_partition(int max_blocks, int bs, int partition_size, int G, bool fp
   return P;
 }
 
+// Clears the decode kernel's item counter.  The decode kernel is its
+// programmatic dependent on eager calls: its CTAs become resident and build
+// their tables while this runs, and wait for it on the device before their
+// first fetch.
+__global__ void __launch_bounds__(32) decode_reset_kernel(int32_t* next) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) *next = 0;
+}
+
+// A launch that may begin before the previous kernel on the stream has
+// completed (programmatic stream serialisation), on eager calls only; under
+// stream capture, or where the attribute is refused, a plain launch.
+cudaError_t launch_dependent(const void* kernel, dim3 grid, dim3 block, void** args, size_t smem,
+                             cudaStream_t stream) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();
+  }
+  return cudaLaunchKernel(kernel, grid, block, args, smem, stream);
+}
+
 }  // namespace
 
 unsigned fetch_status_decode() {
@@ -228,7 +260,7 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num
   if (max_parts <= 1) return 0;
   const long long rows = (long long)num_seqs * num_heads * max_parts;
   const long long ml = ((rows * 2 * 4) + 255) / 256 * 256;
-  return (size_t)(ml + rows * head_dim * 4);
+  return (size_t)(ml + rows * head_dim * 4 + 256);     // + the work-item counter
 }
 
 // Shared by pa_decode and pa_decode_fp8: dtype is the query/output type,
@@ -300,6 +332,8 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   prm.ws_ml = need ? static_cast<float*>(workspace) : nullptr;
   prm.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * 8) + 255) / 256 * 256)
                   : nullptr;
+  // the work-item counter: the workspace's last 256 bytes
+  prm.ws_next = need ? reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + need - 256) : nullptr;
   prm.B = num_seqs;
   prm.Hq = num_heads;
   prm.Hkv = num_kv_heads;
@@ -342,7 +376,8 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
                                      : pick1<__nv_bfloat16, __nv_bfloat16>(head_dim, GT, prm.HG);
   const size_t smem = 2 * (size_t)S * prm.HG * prm.tile_bytes + (fp8 ? 2 * (size_t)S * block_size * 4 : 0) +
                       (size_t)kConsumerWarps * GT * (head_dim + 2) * sizeof(float) +
-                      2 * (size_t)S * sizeof(uint64_t) + 16 +
+                      2 * (size_t)S * sizeof(uint64_t) + 2 * kItemQ * sizeof(uint64_t) + 16 +
+                      (kItemQ + 4) * sizeof(int) +
                       (prm.dense ? 4 * (2 * (size_t)num_seqs + 1 + kThreads / 32) : 0) + kSmemAlign;
   const int occ = occupancy_for(L.kernel, smem, dev);
   if (occ <= 0) return PA_ERR_CUDA;
@@ -350,9 +385,21 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   if (grid > prm.n_virtual) grid = prm.n_virtual;
 
   void* args[] = {&mapK, &mapV, &prm};
-  if (!ck(cudaLaunchKernel(L.kernel, dim3((unsigned)grid), dim3(kThreads), args, smem, (cudaStream_t)stream),
-          "cudaLaunchKernel(decode_kernel)"))
+  if (prm.ws_next && prm.dense) {
+    // items handed out at run time from the counter in the workspace
+    void* rargs[] = {&prm.ws_next};
+    if (!ck(cudaLaunchKernel(reinterpret_cast<const void*>(&decode_reset_kernel), dim3(1), dim3(32), rargs, 0,
+                             (cudaStream_t)stream),
+            "cudaLaunchKernel(decode_reset_kernel)"))
+      return PA_ERR_CUDA;
+    if (!ck(launch_dependent(L.kernel, dim3((unsigned)grid), dim3(kThreads), args, smem, (cudaStream_t)stream),
+            "cudaLaunchKernel(decode_kernel)"))
+      return PA_ERR_CUDA;
+  } else if (!ck(cudaLaunchKernel(L.kernel, dim3((unsigned)grid), dim3(kThreads), args, smem,
+                                  (cudaStream_t)stream),
+                 "cudaLaunchKernel(decode_kernel)")) {
     return PA_ERR_CUDA;
+  }
   if (max_parts > 1) {
     const long long warps = (long long)num_seqs * num_heads;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);

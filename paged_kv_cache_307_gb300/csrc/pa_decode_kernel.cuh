@@ -93,6 +93,7 @@ struct DecodeParams {
   int spg;            // shared-memory stages per warp group
   int spg_shift;      // log2(spg) when spg is a power of two, else -1
   uint32_t tile_bytes;  // one head's K (or V) tile of one block: bs * D * elem
+  int32_t* ws_next;     // item counter in the workspace, zero at launch; null: items by static striding
 };
 
 struct Item {
@@ -104,6 +105,11 @@ struct Item {
 // clamped lengths and the prefix sum of partitions per sequence in shared
 // memory (8 bytes per sequence).
 constexpr int kDenseMaxSeqs = 1024;
+
+// Items handed out at run time (a workspace holds the counter and the
+// enumeration is dense): the producer passes each item index to the consumer
+// warps through a queue of kItemQ slots in shared memory.
+constexpr int kItemQ = 4;
 
 __device__ __forceinline__ void finish_item(const DecodeParams& p, int L, int nparts, Item& it) {
   const int t0 = it.part * p.part_tokens;
@@ -202,9 +208,12 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   float* mbuf = sclV + (SCALED ? S * p.bs : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + NCW * GT * (D + 2));
   uint64_t* empty = full + S;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  uint64_t* qfull = empty + S;                  // [kItemQ] item queue: index written
+  uint64_t* qempty = qfull + kItemQ;            // [kItemQ] item queue: index taken by the consumers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + kItemQ);
+  int* qid = const_cast<int*>(abort_flag) + 4;  // [kItemQ], then the index the consumers work on
   // dense enumeration: partition prefix [B+1], clamped lengths [B], warp sums
-  int* pre = const_cast<int*>(abort_flag) + 4;
+  int* pre = qid + kItemQ + 4;
   int* Ls = pre + (p.dense ? p.B + 1 : 0);
   int* wsum = Ls + (p.dense ? p.B : 0);
 
@@ -218,6 +227,10 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], HG);
+    }
+    for (int q = 0; q < kItemQ; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -256,6 +269,11 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   } else {
     __syncthreads();
   }
+  // Run-time items: each CTA's producer takes the next index from the
+  // counter when it gets to it (the counter is cleared by the kernel launched
+  // just before this one, which this grid may overlap on eager calls: wait
+  // for it before the first fetch).
+  const bool dyn = p.ws_next != nullptr && p.dense;
 
   // An item covers HG KV heads.  Consumer warp w works on head w % HG of
   // the item, in warp group w / HG; block i of the item goes to group
@@ -293,7 +311,34 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     uint32_t base[NCW], issued[NCW];
 #pragma unroll
     for (int w = 0; w < NCW; ++w) base[w] = issued[w] = 0;
-    for (long long v = blockIdx.x; v < n_items; v += gridDim.x) {
+    int pend = 0, kq = 0;
+    if (dyn) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (lane == 0) pend = atomicAdd(p.ws_next, 1);
+    }
+    for (long long v = blockIdx.x;; v += gridDim.x) {
+      if (dyn) {
+        // hand the next index (-1: none left) to the consumers; the one
+        // after it is fetched while this item's loads go out
+        const int q = kq % kItemQ;
+        int nv = -1;
+        if (lane == 0) {
+          if (!*abort_flag && mbar_wait(&qempty[q], ((uint32_t)(kq / kItemQ) & 1u) ^ 1u)) {
+            nv = pend < n_items ? pend : -1;
+            if (nv >= 0) pend = atomicAdd(p.ws_next, 1);
+            qid[q] = nv;
+            mbar_arrive(&qfull[q]);
+          } else if (!*abort_flag) {
+            atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+        }
+        ++kq;
+        v = __shfl_sync(0xffffffffu, nv, 0);
+        if (v < 0) break;
+      } else if (v >= n_items) {
+        break;
+      }
       Item item;
       if (p.dense) dense_item(p, pre, Ls, (int)v, item);
       else if (!decode_item(p, v, item)) continue;
@@ -394,7 +439,41 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   const int hl = warp % HG;       // the item's KV head this warp works on
   const int gw = warp / HG;       // this warp's group
 
-  for (long long v = blockIdx.x; v < n_items; v += gridDim.x) {
+  int kq = 0;
+  volatile int* cur = qid + kItemQ;   // the index every consumer warp works on next
+  for (long long v = blockIdx.x;; v += gridDim.x) {
+    if (dyn) {
+      // Consumer warp 0 takes the producer's next index (-1: none left, or
+      // the pipeline aborted) and every consumer warp reads it after a
+      // barrier, so all of them walk the same items and meet at the same
+      // per-item barriers.
+      if (warp == 0) {
+        const int q = kq % kItemQ;
+        int nv = -1;
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0) {
+          const bool late = !mbar_wait(&qfull[q], (uint32_t)(kq / kItemQ) & 1u);
+          if (__any_sync(0xffffffffu, late)) {
+            if (lane == 0) {
+              atomicOr(&g_status_decode, PA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          } else {
+            nv = qid[q];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          *cur = nv;
+          if (nv >= 0 || *abort_flag == 0) mbar_arrive(&qempty[q]);
+        }
+      }
+      ++kq;
+      named_sync(2, NCW * 32);
+      v = *cur;
+      if (v < 0) break;
+    } else if (v >= n_items) {
+      break;
+    }
     Item item;
     if (p.dense) dense_item(p, pre, Ls, (int)v, item);
     else if (!decode_item(p, v, item)) continue;

@@ -33,7 +33,8 @@ def test_workspace_and_partition_arithmetic(pa):
     assert pa.partition_size(64, 32, 32, 128, 128, 16, 0) == 256
     rows = 64 * 32 * 8
     ml = (rows * 8 + 255) // 256 * 256
-    assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, 0) == ml + rows * 128 * 4
+    # (m, l) pairs, partial outputs, then 256 bytes for the work-item counter
+    assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, 0) == ml + rows * 128 * 4 + 256
     assert pa.workspace_bytes(64, 32, 32, 128, 128, 16, -1) == 0          # never split
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 0) == 12                   # fits one partition
     assert pa.partition_size(1, 8, 8, 32, 3, 4, 6) == -2                   # not a block multiple
