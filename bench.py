@@ -874,7 +874,9 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty_like(case.q)
     stream = torch.cuda.current_stream()
     P = pa.partition_size(Bsz, Hq, spec.Hkv, D, case.max_blocks, spec.bs, args.partition, fp8=fp8)
-    launches_per_step = 4 if shared else 2 + (1 if case.max_blocks * spec.bs > P else 0)
+    # append + decode; a split call adds the merge and, with its workspace
+    # holding the work-item counter, the kernel that clears it
+    launches_per_step = 4 if shared else 2 + (2 if case.max_blocks * spec.bs > P else 0)
 
     # HBM bytes a decode call must move: each physical block once (shared
     # prompt blocks count once; for private blocks this is the logical count)

@@ -94,6 +94,7 @@ struct DecodeParams {
   int spg_shift;      // log2(spg) when spg is a power of two, else -1
   uint32_t tile_bytes;  // one head's K (or V) tile of one block: bs * D * elem
   int32_t* ws_next;     // item counter in the workspace, zero at launch; null: items by static striding
+  int lpt;              // dense order: partial last partitions after all full ones, largest first
 };
 
 struct Item {
@@ -120,26 +121,52 @@ __device__ __forceinline__ void finish_item(const DecodeParams& p, int L, int np
   it.split = nparts > 1;
 }
 
-// Dense item i -> (sequence, partition, KV-head group, query subgroup): the
-// (sequence, partition) units are numbered sequence by sequence, and the
-// n_hg * nsub items of a unit are consecutive, so the CTAs running side by
-// side cover neighbouring sequences (siblings sharing a prompt read the same
-// blocks) and every CTA gets the same number of items up to one.
-__device__ __forceinline__ void dense_item(const DecodeParams& p, const int* pre, const int* Ls, int i, Item& it) {
+// Dense enumeration order, with lpt: every sequence's full partitions first
+// (sequence by sequence), then each sequence's partial last partition,
+// largest first (a stable counting sort on the remainder in kRemBuckets
+// buckets), so the items handed out last are the shortest; without: every
+// sequence's partitions in order, sequence by sequence (short partitions:
+// their fixed per-item cost then stays spread among long items instead of
+// meeting at the end of the launch).  The n_hg * nsub items of a
+// (sequence, partition) unit are consecutive.
+constexpr int kRemBuckets = 64;
+
+// Bucket of a sequence's partial last partition (-1: it has none): larger
+// remainders first, an empty sequence (its one empty unit) last.
+__device__ __forceinline__ int rem_bucket(int L, int P) {
+  const int rem = L - (L / P) * P;
+  if (L > 0 && rem == 0) return -1;
+  return kRemBuckets - 1 - min(kRemBuckets - 1, (int)((long long)rem * kRemBuckets / P));
+}
+
+// Dense item i -> (sequence, partition, KV-head group, query subgroup).
+// pre[b]: the units of the sequences before b in the first class (their
+// full partitions with lpt, all their partitions without; pre[B] = NF);
+// perm: with lpt, the sequences with a partial last partition in the order
+// above.
+__device__ __forceinline__ void dense_item(const DecodeParams& p, const int* pre, const int* perm, const int* Ls,
+                                           int i, Item& it) {
   const int nper = p.n_hg * p.nsub;
   const int u = i / nper;
   const int r = i - u * nper;
   it.kvh0 = (r % p.n_hg) * p.HG;
   it.sg = r / p.n_hg;
-  int lo = 0, hi = p.B - 1;       // the last sequence whose first unit is <= u
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pre[mid] <= u) lo = mid;
-    else hi = mid - 1;
+  const int NF = pre[p.B];
+  if (u < NF) {
+    int lo = 0, hi = p.B - 1;       // the last sequence whose first full unit is <= u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    it.b = lo;
+    it.part = u - pre[lo];
+  } else {
+    it.b = perm[u - NF];
+    it.part = Ls[it.b] / p.part_tokens;
   }
-  it.b = lo;
-  it.part = u - pre[lo];
-  finish_item(p, Ls[lo], pre[lo + 1] - pre[lo], it);
+  const int L = Ls[it.b];
+  finish_item(p, L, L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1, it);
 }
 
 __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long v, Item& it) {
@@ -215,7 +242,9 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   // dense enumeration: partition prefix [B+1], clamped lengths [B], warp sums
   int* pre = qid + kItemQ + 4;
   int* Ls = pre + (p.dense ? p.B + 1 : 0);
-  int* wsum = Ls + (p.dense ? p.B : 0);
+  int* perm = Ls + (p.dense ? p.B : 0);          // [B] partial last partitions, largest first
+  int* hist = perm + (p.dense ? p.B : 0);        // [kRemBuckets * NW + 1] per (bucket, warp) counts
+  int* wsum = hist + (p.dense ? kRemBuckets * (kThreads / 32) + 1 : 0);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -238,8 +267,15 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   long long n_items = p.n_virtual;
   if (p.dense) {
     // Every CTA builds the same tables: each thread takes a contiguous run
-    // of sequences, then a block-wide exclusive scan of the run totals.
+    // of sequences, then a block-wide exclusive scan of the run totals (full
+    // partitions per sequence); then a stable counting sort of the
+    // sequences with a partial last partition, each warp counting and then
+    // placing a contiguous range of sequences (no atomics: every CTA gets the
+    // same permutation).
+    constexpr int NW = kThreads / 32;
     const int Lmax = p.max_blocks * p.bs;
+    const int P = p.part_tokens;
+    for (int i = threadIdx.x; i <= kRemBuckets * NW; i += kThreads) hist[i] = 0;
     const int per = (p.B + kThreads - 1) / kThreads;
     const int b0 = min(p.B, (int)threadIdx.x * per), b1 = min(p.B, b0 + per);
     int sum = 0;
@@ -247,7 +283,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
       int L = __ldg(&p.context_lens[b]);
       if (L < 0 || L > Lmax) L = L < 0 ? 0 : Lmax;   // flagged by the consumer
       Ls[b] = L;
-      sum += L > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+      sum += p.lpt ? L / P : (L > 0 ? (L + P - 1) / P : 1);
     }
     int incl = sum;
 #pragma unroll
@@ -261,11 +297,54 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
     for (int w = 0; w < warp; ++w) run += wsum[w];
     for (int b = b0; b < b1; ++b) {
       pre[b] = run;
-      run += Ls[b] > 0 ? (Ls[b] + p.part_tokens - 1) / p.part_tokens : 1;
+      run += p.lpt ? Ls[b] / P : (Ls[b] > 0 ? (Ls[b] + P - 1) / P : 1);
     }
     if (threadIdx.x == kThreads - 1) pre[p.B] = run;
+    // counts per (bucket, warp) over each warp's range
+    const int chunk = (p.B + NW - 1) / NW;
+    const int r0 = warp * chunk, r1 = p.lpt ? min(p.B, r0 + chunk) : r0;
+    for (int base = r0; base < r1; base += 32) {
+      const int b = base + lane;
+      const int d = b < r1 ? rem_bucket(Ls[b], P) : -1;
+      const unsigned m = __match_any_sync(0xffffffffu, d);
+      if (d >= 0 && (m & ((1u << lane) - 1u)) == 0) hist[d * NW + warp] += __popc(m);
+      __syncwarp();
+    }
     __syncthreads();
-    n_items = (long long)pre[p.B] * p.n_hg * p.nsub;
+    // exclusive scan of the counts (bucket-major, then warp): warp 0
+    if (p.lpt && warp == 0) {
+      int carry = 0;
+      for (int i0 = 0; i0 < kRemBuckets * NW; i0 += 32) {
+        const int c = i0 + lane < kRemBuckets * NW ? hist[i0 + lane] : 0;
+        int x = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        if (i0 + lane < kRemBuckets * NW) hist[i0 + lane] = carry + x - c;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) hist[kRemBuckets * NW] = carry;
+    }
+    __syncthreads();
+    const int nR = hist[kRemBuckets * NW];
+    for (int base = r0; base < r1; base += 32) {
+      const int b = base + lane;
+      const int d = b < r1 ? rem_bucket(Ls[b], P) : -1;
+      const unsigned m = __match_any_sync(0xffffffffu, d);
+      const int rank = __popc(m & ((1u << lane) - 1u));
+      int pos = 0;
+      if (d >= 0) pos = hist[d * NW + warp] + rank;
+      __syncwarp();
+      if (d >= 0) {
+        perm[pos] = b;
+        if (rank == 0) hist[d * NW + warp] += __popc(m);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    n_items = (long long)(pre[p.B] + nR) * p.n_hg * p.nsub;
   } else {
     __syncthreads();
   }
@@ -340,7 +419,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
         break;
       }
       Item item;
-      if (p.dense) dense_item(p, pre, Ls, (int)v, item);
+      if (p.dense) dense_item(p, pre, perm, Ls, (int)v, item);
       else if (!decode_item(p, v, item)) continue;
       const int32_t* row = p.block_tables + (size_t)item.b * p.max_blocks;
       const int nblk = item.je - item.jb;
@@ -475,7 +554,7 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
       break;
     }
     Item item;
-    if (p.dense) dense_item(p, pre, Ls, (int)v, item);
+    if (p.dense) dense_item(p, pre, perm, Ls, (int)v, item);
     else if (!decode_item(p, v, item)) continue;
     if (ctid == 0 && item.kvh0 == 0 && item.sg == 0 && item.part == 0) {
       const int L = __ldg(&p.context_lens[item.b]);
