@@ -136,7 +136,13 @@ int pa_reshape_and_cache(const void* key, const void* value,
  *   workspace      device scratch of at least pa_decode_workspace_bytes()
  *                  with the same sizes (may be NULL when that is 0).  Its
  *                  contents on entry do not matter; calls that share one
- *                  workspace must be ordered (same stream).
+ *                  workspace must be ordered (same stream).  Its last 256
+ *                  bytes hold a work-item counter: a one-thread kernel clears
+ *                  it, then the decode kernel's CTAs take their work items
+ *                  from it as they free up (on eager calls the decode kernel
+ *                  is that kernel's programmatic dependent and waits for it
+ *                  on the device).  Without a workspace (no split needed) the
+ *                  items are divided among the CTAs in advance.
  *
  * Output is fp32-accumulated; bf16 output is rounded to nearest even.  With
  * bf16, head_dim 64 or 128, block_size >= 8 and a power-of-two group G >= 2,
