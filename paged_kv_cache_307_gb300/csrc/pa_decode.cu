@@ -366,6 +366,10 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
   int spg = (int)(budget / (2 * prm.tile_bytes * kConsumerWarps));
   spg = spg < 1 ? 1 : (spg > PA_MAX_STAGES_PER_GROUP ? PA_MAX_STAGES_PER_GROUP : spg);
   while (!use_mma && (spg & (spg - 1))) spg &= spg - 1;   // CUDA-core path: a power of two
+  // e4m3 tensor-core path: three stages per group, so that three CTAs fit on
+  // an SM beside the dense tables of up to 1024 sequences (four stages of
+  // 8 KB left room for two at 256 sequences)
+  if (use_mma && kv == PA_FP8_E4M3 && spg > 3) spg = 3;
   if (prm.WPH == 1) {
     const size_t stage = 2 * (size_t)prm.HG * prm.tile_bytes;
     if (spg < 2) spg = 2;
@@ -383,10 +387,7 @@ static int decode_impl(void* out, const void* query, const void* k_cache, const 
                       (size_t)kConsumerWarps * GT * (head_dim + 2) * sizeof(float) +
                       2 * (size_t)S * sizeof(uint64_t) + 2 * kItemQ * sizeof(uint64_t) + 16 +
                       (kItemQ + 4) * sizeof(int) +
-                      (prm.dense ? 4 * (3 * (size_t)num_seqs + 1 + kRemBuckets * (kThreads / 32) + 1 +
-                                        kThreads / 32)
-                                 : 0) +
-                      kSmemAlign;
+                      (prm.dense ? 4 * (3 * (size_t)num_seqs + 1 + kThreads / 32) : 0) + kSmemAlign;
   const int occ = occupancy_for(L.kernel, smem, dev);
   if (occ <= 0) return PA_ERR_CUDA;
   long long grid = (long long)occ * device_sm_count();

@@ -243,8 +243,10 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
   int* pre = qid + kItemQ + 4;
   int* Ls = pre + (p.dense ? p.B + 1 : 0);
   int* perm = Ls + (p.dense ? p.B : 0);          // [B] partial last partitions, largest first
-  int* hist = perm + (p.dense ? p.B : 0);        // [kRemBuckets * NW + 1] per (bucket, warp) counts
-  int* wsum = hist + (p.dense ? kRemBuckets * (kThreads / 32) + 1 : 0);
+  int* wsum = perm + (p.dense ? p.B : 0);
+  // [kRemBuckets * NW + 1] per (bucket, warp) counts while the tables are
+  // built: scratch in the K stages, which no copy fills before then
+  int* hist = reinterpret_cast<int*>(tilesK);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -343,6 +345,9 @@ decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ 
       }
       __syncwarp();
     }
+    // order these generic writes to the stage memory before the TMA copies
+    // that will overwrite it
+    fence_proxy_async_smem();
     __syncthreads();
     n_items = (long long)(pre[p.B] + nR) * p.n_hg * p.nsub;
   } else {
