@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--long-repeat", type=int, default=2000,
+                    help="decode legs: steps of the event-free repeat after a shorter timed region (0: none)")
     ap.add_argument("--no-share", action="store_true",
                     help="c5: run plain pa_decode instead of the shared-prefix path")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -949,7 +951,7 @@ def run_ours(args, rank, world, local_rank):
     # K-step region: a steadier step time and a fuller clock record when K is
     # small (the line's value stays the K-step one)
     repeat_line = None
-    R = max(K, 2000)
+    R = max(K, args.long_repeat)
     if R > K:
         ra, rb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         rs = ClockSampler(sampler.index)
